@@ -1,0 +1,154 @@
+/*
+ * strata_window.h -- C ABI of a GB300 (sm_103a) library that runs the batched
+ * verify-window MoE decode step.
+ *
+ * What a window is (the Strata docs, "BATCHING.md", section "Several requests
+ * at once (batch slots)", opening paragraph): every verify window carries one
+ * token of each open conversation, so the dense weights, the shared expert and
+ * every routed expert two conversations share are read once per window for all
+ * of them.  A window holds at most 8 rows (same page, option table: "a window
+ * holds 8 rows"); with --batch-mtp each slot adds its MTP proposal as a second
+ * row (same page, --batch-mtp paragraph).  Section "Exactness": a batch row's
+ * arithmetic is the single-token window's.
+ *
+ * One MoE layer of a window, as this library computes it (the pages give no
+ * formulas; these are the readings the library implements):
+ *   logit[t][e] = sum_j Wr[e][j] x[t][j] + b[e]                 (fp32)
+ *   p[t]        = softmax(logit[t]) over all E experts           (fp32)
+ *   sel[t]      = the top_k experts by logit, descending, ties to the lower id
+ *   g[t][j]     = p[t][sel[t][j]]  (or renormalised over the k when renorm_topk)
+ *   h           = silu(Wg_e x_t) * (Wu_e x_t),  silu(z) = z / (1 + e^-z)
+ *   y[t]        = shared(x_t) + sum_j g[t][j] * Wd_e h          (e = sel[t][j])
+ * where shared() is the same SwiGLU FFN with weight 1 and no gate.
+ *
+ * Block format of a quantized matrix [rows][cols]: blocks of `block` elements
+ * along cols; per block `block*bits/8` code bytes (element i of a row in byte
+ * i*bits/8, least-significant bits first: for 4-bit the even element is the
+ * low nibble), one fp16 scale and one fp16 min; weight = scale*q + min.  Codes
+ * are row-major [rows][cols*bits/8]; scale and min are fp16 bit patterns
+ * [rows][cols/block].  Supported: bits=4 with block=32, bits=2 with block=16.
+ *
+ * Errors: every call returns a status and never aborts.  Argument errors are
+ * found on the host before any GPU work.  Errors the GPU detects (a bounded
+ * wait that gave up, an index guard, a non-finite router logit) are recorded
+ * in a device error word and returned by the next strata_window_sync().
+ */
+#ifndef STRATA_WINDOW_H
+#define STRATA_WINDOW_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  STRATA_OK = 0,
+  STRATA_EINVAL = 1,        /* a bad argument; nothing was launched */
+  STRATA_ENOMEM = 2,        /* a device allocation failed */
+  STRATA_ECUDA = 3,         /* a CUDA runtime call failed */
+  STRATA_EUNSUPPORTED = 4,  /* a valid but unsupported shape or format */
+  STRATA_EDEVICE = 5        /* the GPU flagged an error during an earlier call */
+} strata_status;
+
+typedef struct strata_window strata_window; /* opaque handle */
+
+/* One stack of quantized matrices in the block format above.  All three are
+ * device pointers.  For a stack of n matrices the arrays are the n matrices
+ * back to back ([n][rows][...]). */
+typedef struct {
+  const void* codes;      /* uint8 [n][rows][cols*bits/8] */
+  const uint16_t* scale;  /* fp16 bits [n][rows][cols/block] */
+  const uint16_t* min;    /* fp16 bits [n][rows][cols/block] */
+} strata_qmat;
+
+/* Shape of one MoE layer. */
+typedef struct {
+  int32_t hidden;       /* d: multiple of 64 (4-bit) or 128 (2-bit) */
+  int32_t n_experts;    /* E: 1..256 */
+  int32_t top_k;        /* k: 1..min(E, 8) */
+  int32_t ffn;          /* F: routed expert width, multiple of 64 (4-bit) or 128 (2-bit) */
+  int32_t shared_ffn;   /* Fs: shared expert width (same rule), 0 = no shared expert */
+  int32_t bits;         /* 4 or 2 */
+  int32_t block;        /* 32 (with bits=4) or 16 (with bits=2) */
+  int32_t max_rows;     /* largest window this handle serves: 1..8 */
+  int32_t renorm_topk;  /* 0: gate = softmax prob over all E; 1: renormalised over the k */
+} strata_moe_desc;
+
+/* Weights of one layer (device pointers).  They are read during
+ * strata_window_create only: create copies them into the handle's own
+ * kernel-ordered layout, so the caller may free them once create returns. */
+typedef struct {
+  const float* router_w;    /* fp32 [E][d] */
+  const float* router_b;    /* fp32 [E], or NULL for no bias */
+  strata_qmat gate;         /* [E][F][d] */
+  strata_qmat up;           /* [E][F][d] */
+  strata_qmat down;         /* [E][d][F] */
+  strata_qmat shared_gate;  /* [1][Fs][d]  (ignored when shared_ffn == 0) */
+  strata_qmat shared_up;    /* [1][Fs][d] */
+  strata_qmat shared_down;  /* [1][d][Fs] */
+} strata_moe_weights;
+
+/* Optional routing outputs of a forward call (device pointers; each may be
+ * NULL).  Entries are numbered t*k + j (row t, j-th selected expert). */
+typedef struct {
+  int32_t* topk_idx;    /* [T][k] selected experts, descending logit */
+  float* topk_w;        /* [T][k] gate weights */
+  int32_t* counts;      /* [E] entries per expert */
+  int32_t* offsets;     /* [E+1] exclusive prefix sum of counts */
+  int32_t* entries;     /* [T*k] entries grouped by expert (ascending), ascending within an expert */
+  int32_t* distinct;    /* [E] experts with count > 0, ascending (first n_distinct valid) */
+  int32_t* n_distinct;  /* [1] */
+} strata_routing_out;
+
+/* Sizes a handle chose (for measurement and tests). */
+typedef struct {
+  int32_t n_sm;               /* SMs of the device (grid of the expert kernels) */
+  int32_t stages_gateup;      /* shared-memory ring stages of the gate/up kernel */
+  int32_t stages_down;        /* ... of the down kernel */
+  int32_t smem_gateup;        /* dynamic shared memory bytes per CTA */
+  int32_t smem_down;
+  int64_t packed_bytes;       /* bytes of the handle's kernel-ordered weights */
+  int64_t expert_bytes;       /* block-format bytes of one routed expert (gate+up+down) */
+  int64_t shared_bytes;       /* block-format bytes of the shared expert */
+  int64_t router_bytes;       /* router weight (+ bias) bytes */
+  int64_t workspace_bytes;    /* handle scratch bytes */
+} strata_window_info;
+
+/* Create a handle for one MoE layer on the current CUDA device.
+ *   desc, weights: as above; weights are read on `cuda_stream` (a cudaStream_t,
+ *   or NULL for the default stream) and create waits for that work to finish.
+ *   out: receives the handle; set to NULL on failure.
+ * Returns EINVAL (bad pointer or shape), EUNSUPPORTED (bits/block pair or size
+ * limits), ENOMEM, ECUDA. */
+strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe_weights* weights,
+                                   void* cuda_stream, strata_window** out);
+
+/* Run one window: y = MoE(x) for T rows.
+ *   x: device fp32 [T][d], caller-owned; y: device fp32 [T][d], caller-owned,
+ *   must not overlap x.  1 <= T <= desc.max_rows.
+ *   routing: NULL, or a struct of optional device outputs.
+ *   cuda_stream: the stream to enqueue on (NULL = default stream).
+ * Asynchronous: returns once the work is enqueued.  One handle serves one
+ * stream at a time (calls on the same handle must not overlap on the GPU). */
+strata_status strata_moe_window_forward(strata_window* h, const float* x, int32_t T, float* y,
+                                        const strata_routing_out* routing, void* cuda_stream);
+
+/* Wait for the handle's last forward call to finish; report (and clear) any
+ * error the GPU recorded: EDEVICE in that case. */
+strata_status strata_window_sync(strata_window* h);
+
+/* Fill *info with the sizes the handle chose. */
+strata_status strata_window_query(const strata_window* h, strata_window_info* info);
+
+/* Free the handle and everything it owns.  NULL is accepted (returns OK). */
+strata_status strata_window_destroy(strata_window* h);
+
+/* A static, human-readable name of a status. */
+const char* strata_status_str(strata_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STRATA_WINDOW_H */

@@ -1,0 +1,211 @@
+"""Thin ctypes binding of ``include/strata_window.h``.
+
+Argument marshalling only: the functions keep the C names
+(``strata_window_create``, ``strata_moe_window_forward``, ``strata_window_sync``,
+``strata_window_query``, ``strata_window_destroy``, ``strata_status_str``) and
+every step of a window runs in the library's CUDA kernels.  Loading fails
+loudly when the shared library has not been built; there is no fallback.
+
+``Window`` wraps a handle for torch tensors (device memory and streams come
+from PyTorch; nothing is computed by it).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libstrata_window.so")
+
+STRATA_OK, STRATA_EINVAL, STRATA_ENOMEM, STRATA_ECUDA, STRATA_EUNSUPPORTED, STRATA_EDEVICE = range(6)
+
+EXPORTED = ("strata_window_create", "strata_moe_window_forward", "strata_window_sync", "strata_window_query",
+            "strata_window_destroy", "strata_status_str")
+
+
+class StrataError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_str(status)} ({status})")
+        self.status = status
+
+
+class strata_qmat(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("min", ctypes.c_void_p)]
+
+
+class strata_moe_desc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("hidden", "n_experts", "top_k", "ffn", "shared_ffn", "bits", "block",
+                                              "max_rows", "renorm_topk")]
+
+
+class strata_moe_weights(ctypes.Structure):
+    _fields_ = [("router_w", ctypes.c_void_p), ("router_b", ctypes.c_void_p), ("gate", strata_qmat),
+                ("up", strata_qmat), ("down", strata_qmat), ("shared_gate", strata_qmat),
+                ("shared_up", strata_qmat), ("shared_down", strata_qmat)]
+
+
+class strata_routing_out(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("topk_idx", "topk_w", "counts", "offsets", "entries", "distinct",
+                                               "n_distinct")]
+
+
+class strata_window_info(ctypes.Structure):
+    _fields_ = [("n_sm", ctypes.c_int32), ("stages_gateup", ctypes.c_int32), ("stages_down", ctypes.c_int32),
+                ("smem_gateup", ctypes.c_int32), ("smem_down", ctypes.c_int32), ("packed_bytes", ctypes.c_int64),
+                ("expert_bytes", ctypes.c_int64), ("shared_bytes", ctypes.c_int64), ("router_bytes", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with slot_decode_window_gb300.build.build() "
+                           "(the window step has no non-CUDA implementation)")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    lib.strata_window_create.argtypes = [P(strata_moe_desc), P(strata_moe_weights), ctypes.c_void_p,
+                                         P(ctypes.c_void_p)]
+    lib.strata_window_create.restype = ctypes.c_int
+    lib.strata_moe_window_forward.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                              P(strata_routing_out), ctypes.c_void_p]
+    lib.strata_moe_window_forward.restype = ctypes.c_int
+    lib.strata_window_sync.argtypes = [ctypes.c_void_p]
+    lib.strata_window_sync.restype = ctypes.c_int
+    lib.strata_window_query.argtypes = [ctypes.c_void_p, P(strata_window_info)]
+    lib.strata_window_query.restype = ctypes.c_int
+    lib.strata_window_destroy.argtypes = [ctypes.c_void_p]
+    lib.strata_window_destroy.restype = ctypes.c_int
+    lib.strata_status_str.argtypes = [ctypes.c_int]
+    lib.strata_status_str.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_str(status: int) -> str:
+    return load().strata_status_str(status).decode()
+
+
+# --- the C calls, same names ---------------------------------------------------
+
+
+def strata_window_create(desc: strata_moe_desc, weights: strata_moe_weights, stream: int = 0):
+    """Returns (status, handle or None)."""
+    h = ctypes.c_void_p()
+    st = load().strata_window_create(ctypes.byref(desc), ctypes.byref(weights), ctypes.c_void_p(stream),
+                                     ctypes.byref(h))
+    return st, (h.value if st == STRATA_OK else None)
+
+
+def strata_moe_window_forward(handle, x_ptr: int, T: int, y_ptr: int, routing: Optional[strata_routing_out] = None,
+                              stream: int = 0) -> int:
+    return load().strata_moe_window_forward(ctypes.c_void_p(handle), ctypes.c_void_p(x_ptr), T,
+                                            ctypes.c_void_p(y_ptr),
+                                            ctypes.byref(routing) if routing is not None else None,
+                                            ctypes.c_void_p(stream))
+
+
+def strata_window_sync(handle) -> int:
+    return load().strata_window_sync(ctypes.c_void_p(handle))
+
+
+def strata_window_query(handle):
+    info = strata_window_info()
+    st = load().strata_window_query(ctypes.c_void_p(handle), ctypes.byref(info))
+    return st, info
+
+
+def strata_window_destroy(handle) -> int:
+    return load().strata_window_destroy(ctypes.c_void_p(handle))
+
+
+def check(status: int, what: str) -> None:
+    if status != STRATA_OK:
+        raise StrataError(status, what)
+
+
+# --- torch convenience -----------------------------------------------------------
+
+
+def _qmat(q) -> strata_qmat:
+    return strata_qmat(q.codes.data_ptr(), q.scale.data_ptr(), q.min.data_ptr())
+
+
+def desc_of(spec, max_rows: int = 8) -> strata_moe_desc:
+    return strata_moe_desc(spec.hidden, spec.n_experts, spec.top_k, spec.ffn, spec.shared_ffn, spec.bits, spec.block,
+                           max_rows, spec.renorm_topk)
+
+
+def weights_of(layer) -> strata_moe_weights:
+    w = strata_moe_weights()
+    w.router_w = layer.router_w.data_ptr()
+    w.router_b = layer.router_b.data_ptr() if layer.router_b is not None else None
+    w.gate, w.up, w.down = _qmat(layer.gate), _qmat(layer.up), _qmat(layer.down)
+    if layer.shared_gate is not None:
+        w.shared_gate, w.shared_up, w.shared_down = (_qmat(layer.shared_gate), _qmat(layer.shared_up),
+                                                     _qmat(layer.shared_down))
+    return w
+
+
+class Window:
+    """A handle for one MoE layer whose weights are CUDA torch tensors."""
+
+    def __init__(self, layer, max_rows: int = 8, stream=None):
+        import torch
+        self.spec = layer.spec
+        self.max_rows = max_rows
+        s = (stream or torch.cuda.current_stream()).cuda_stream
+        st, h = strata_window_create(desc_of(layer.spec, max_rows), weights_of(layer), s)
+        check(st, "strata_window_create")
+        self.handle = h
+
+    def info(self) -> strata_window_info:
+        st, info = strata_window_query(self.handle)
+        check(st, "strata_window_query")
+        return info
+
+    def forward(self, x, y=None, routing: bool = False, stream=None):
+        """Enqueue one window on x [T][d] (CUDA fp32); returns y (and routing tensors)."""
+        import torch
+        assert x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()
+        T, d = x.shape
+        if y is None:
+            y = torch.empty_like(x)
+        r = None
+        rt = None
+        if routing:
+            E, k = self.spec.n_experts, self.spec.top_k
+            dev = x.device
+            rt = dict(topk_idx=torch.empty(T, k, dtype=torch.int32, device=dev),
+                      topk_w=torch.empty(T, k, dtype=torch.float32, device=dev),
+                      counts=torch.empty(E, dtype=torch.int32, device=dev),
+                      offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                      entries=torch.empty(T * k, dtype=torch.int32, device=dev),
+                      distinct=torch.full((E,), -1, dtype=torch.int32, device=dev),
+                      n_distinct=torch.empty(1, dtype=torch.int32, device=dev))
+            r = strata_routing_out(*(rt[n].data_ptr() for n in ("topk_idx", "topk_w", "counts", "offsets", "entries",
+                                                               "distinct", "n_distinct")))
+        s = (stream or torch.cuda.current_stream()).cuda_stream
+        check(strata_moe_window_forward(self.handle, x.data_ptr(), T, y.data_ptr(), r, s),
+              "strata_moe_window_forward")
+        return (y, rt) if routing else y
+
+    def sync(self) -> None:
+        check(strata_window_sync(self.handle), "strata_window_sync")
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            strata_window_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,227 @@
+// Device-side definitions shared by the window kernels: packed tile format,
+// window workspace layout, and thin PTX wrappers (mbarrier, bulk async copy,
+// programmatic dependent launch, mma.sync, lop3).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+
+namespace strata {
+
+constexpr int kMaxRows = 8;       // a verify window holds at most 8 rows
+constexpr int kMaxTopK = 8;
+constexpr int kMaxExperts = 256;
+constexpr int kMaxEntries = kMaxRows * kMaxTopK;
+constexpr int kConsumerWarps = 8;
+constexpr int kExpertThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kRouterThreads = 256;
+constexpr int kMaxStages = 8;
+
+// Bits of the device error word.
+enum : uint32_t {
+  kErrTimeout = 1u,     // a bounded wait gave up
+  kErrIndex = 2u,       // an index derived from routing was out of range
+  kErrNonFinite = 4u,   // a router logit was not finite
+  kErrConfig = 8u,      // a launch saw an impossible configuration
+};
+
+// ---------------------------------------------------------------------------
+// Packed tile format.
+//
+// A quantized matrix [rows][K] (rows % 16 == 0, K % kstep == 0) is stored as
+// rows/16 tiles of 16 rows.  A tile is nks "k-steps" followed by nmk min
+// fragments:
+//   k-step (576 B for 4-bit, 768 B for 2-bit):
+//     512 B codes: 32 lanes x 16 B, lane (g = lane/4, c = lane%4) holds the
+//                  A-operand codes of rows g and g+8 for its k-slots;
+//     scales: 8 records (one per g): 4-bit: s(g,b0) s(g,b1) s(g+8,b0) s(g+8,b1)
+//             2-bit: s(g,b0..b7) then s(g+8,b0..b7)   (fp16)
+//   min fragment (512 B per 16 blocks): lane (g,c) holds the mins of rows
+//     g, g+8 for blocks 2c, 2c+1, 2c+8, 2c+9 in mma A-fragment order (fp16,
+//     blocks past the end are zero).
+// Code words: each 32-bit word holds pairs of codes at bits (p, p+16) so that
+// one lop3 against 0x64006400 yields an fp16x2 of (1024 + f*q) values.
+//   4-bit word (one row, one block, lane c covers elements 8c..8c+7):
+//     bits 0/16: e0,e1   4/20: e2,e3 (x16)   8/24: e4,e5   12/28: e6,e7 (x16)
+//   2-bit word (rows g and g+8, two blocks b0,b1, lane c covers elements 4c..4c+3):
+//     pair p at bits (2p, 2p+16): p=0 g/b0 e0,e1; p=1 g/b0 e2,e3 (x4);
+//     p=2 g/b1 e0,e1 (x16); p=3 g/b1 e2,e3 (x64); p=4..7 the same for row g+8.
+// The activation (B operand) records carry the inverse power-of-two factors.
+// ---------------------------------------------------------------------------
+template <int BITS> struct Fmt;
+template <> struct Fmt<4> {
+  static constexpr int kBlock = 32, kKstep = 64, kBlocksPerKstep = 2;
+  static constexpr int kScaleRec = 8;      // bytes per g in a k-step
+  static constexpr int kChunk = 512 + 8 * kScaleRec;   // 576
+  static constexpr int kBHalves = 16;      // B halves per (k-step, lane c)
+};
+template <> struct Fmt<2> {
+  static constexpr int kBlock = 16, kKstep = 128, kBlocksPerKstep = 8;
+  static constexpr int kScaleRec = 32;
+  static constexpr int kChunk = 512 + 8 * kScaleRec;   // 768
+  static constexpr int kBHalves = 32;
+};
+
+// One packed matrix stack [n][rows][K].
+struct PackedMat {
+  const uint8_t* base;
+  int rows, K, nks, nmk;
+  int tile_bytes;          // nks*chunk + nmk*512
+  long long mat_bytes;     // (rows/16) * tile_bytes
+};
+
+// Activation fragments of one vector of length K:
+//   main hi [nks][4][S] halves, main lo [nks][4][S], sums hi [nmk][4][4],
+//   sums lo [nmk][4][4].  Size in halves: 2*K + 32*nmk.
+__host__ __device__ inline long long frag_halves(int K, int nmk) { return 2LL * K + 32LL * nmk; }
+
+// Routing plan written by the router kernel's last CTA.
+struct Plan {
+  int n_distinct;
+  int T;
+  int distinct[kMaxExperts];
+  int counts[kMaxExperts];
+  int offsets[kMaxExperts + 1];
+  int entries[kMaxEntries];
+  int topk_idx[kMaxEntries];
+  float topk_w[kMaxEntries];
+};
+
+struct LayerDev {
+  int d, E, k, F, Fs, bits, renorm;
+  const float* router_w;   // [E][d]
+  const float* router_b;   // [E] or null
+  PackedMat gate, up, down, sgate, sup, sdown;
+};
+
+struct WindowBufs {
+  const float* x;          // [T][d]
+  float* y;                // [T][d]
+  int T;
+  // caller's optional routing outputs (device pointers, each may be null)
+  int* out_topk_idx; float* out_topk_w; int* out_counts; int* out_offsets;
+  int* out_entries; int* out_distinct; int* out_ndistinct;
+  // workspace
+  float* logits;           // [kMaxRows][E]
+  Plan* plan;
+  __half* xfrag;           // [kMaxRows][frag(d)]
+  __half* hfrag;           // [kMaxEntries][frag(F)]
+  __half* shfrag;          // [kMaxRows][frag(Fs)]
+  float* hpart;            // [kMaxEntries][F/16]
+  float* shpart;           // [kMaxRows][Fs/16]
+  float* obuf;             // [kMaxEntries][d]
+  float* sbuf;             // [kMaxRows][d]
+  int* counters;           // [d/16]
+  unsigned* ticket;
+  unsigned* err;
+};
+
+// Shared-memory plan of an expert kernel launch.
+struct SmemCfg {
+  int nstages;
+  int stage_bytes;         // max tile bytes of the matrices streamed
+  int bmain_halves;        // B main halves per set: nks_max*8*4*S
+  int bsum_halves;         // B sums halves per set: nmk_max*8*4*4
+  int nsets;               // 1 (rows <= 4) or 2
+  int total_bytes;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: gives up after ~2^31 cycles (about a second), sets the error
+// word and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > (1LL << 31)) {
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Bulk async copy global -> this CTA's shared memory, completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Named barrier among the consumer warps only (the producer warp keeps running).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// (1024 + f*q) pair -> exact f*q pair in fp16.
+__device__ __forceinline__ uint32_t dq_pair(uint32_t w, uint32_t mask) {
+  return hsub2_u32(lop3_and_or(w, mask, 0x64006400u), 0x64006400u);
+}
+
+// D = A * B + C, m16n8k16, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1, const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// hi = fp16(v), lo = fp16(v - hi)
+__device__ __forceinline__ void split_hi_lo(float v, __half& hi, __half& lo) {
+  hi = __float2half_rn(v);
+  lo = __float2half_rn(v - __half2float(hi));
+}
+
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace strata

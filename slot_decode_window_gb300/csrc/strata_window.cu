@@ -1,0 +1,313 @@
+// C ABI of the verify-window MoE step: argument checks, the handle's memory
+// (kernel-ordered weights + window workspace), and the per-window launch
+// sequence router -> gate/up -> down+combine (programmatic dependent launch
+// between them).
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "strata_window.h"
+
+using namespace strata;
+
+struct strata_window {
+  strata_moe_desc desc;
+  int device = 0;
+  int nsm = 0;
+  LayerDev L{};
+  WindowBufs W{};
+  SmemCfg c_gateup{}, c_down{};
+  float* partial = nullptr;
+  void* wmem = nullptr;
+  void* ws = nullptr;
+  long long packed = 0, ws_bytes = 0;
+  cudaEvent_t done = nullptr;
+};
+
+namespace {
+
+bool fault_is(const char* what) {
+  const char* f = std::getenv("STRATA_FAULT");
+  return f && std::strcmp(f, what) == 0;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int kstep_of(int bits) { return bits == 4 ? 64 : 128; }
+
+strata_status check_desc(const strata_moe_desc* d) {
+  if (!d) return STRATA_EINVAL;
+  if (d->hidden <= 0 || d->n_experts <= 0 || d->top_k <= 0 || d->ffn <= 0 || d->shared_ffn < 0 || d->max_rows <= 0)
+    return STRATA_EINVAL;
+  if (d->top_k > d->n_experts) return STRATA_EINVAL;
+  if (d->renorm_topk != 0 && d->renorm_topk != 1) return STRATA_EINVAL;
+  if (d->max_rows > kMaxRows) return STRATA_EINVAL;
+  if (!((d->bits == 4 && d->block == 32) || (d->bits == 2 && d->block == 16))) return STRATA_EUNSUPPORTED;
+  if (d->n_experts > kMaxExperts || d->top_k > kMaxTopK) return STRATA_EUNSUPPORTED;
+  const int ks = kstep_of(d->bits);
+  if (d->hidden % ks != 0 || d->ffn % ks != 0 || (d->shared_ffn > 0 && d->shared_ffn % ks != 0))
+    return STRATA_EUNSUPPORTED;
+  if (d->hidden > 16384 || d->ffn > 16384 || d->shared_ffn > 16384) return STRATA_EUNSUPPORTED;
+  return STRATA_OK;
+}
+
+bool qmat_ok(const strata_qmat& q) { return q.codes && q.scale && q.min; }
+
+strata_status check_weights(const strata_moe_desc* d, const strata_moe_weights* w) {
+  if (!w) return STRATA_EINVAL;
+  if (!w->router_w || !qmat_ok(w->gate) || !qmat_ok(w->up) || !qmat_ok(w->down)) return STRATA_EINVAL;
+  if (d->shared_ffn > 0 && (!qmat_ok(w->shared_gate) || !qmat_ok(w->shared_up) || !qmat_ok(w->shared_down)))
+    return STRATA_EINVAL;
+  return STRATA_OK;
+}
+
+long long qmat_bytes(int n, int rows, int cols, int bits, int block) {
+  return (long long)n * rows * ((long long)cols * bits / 8 + 4LL * (cols / block));
+}
+
+void free_handle(strata_window* h) {
+  if (!h) return;
+  if (h->done) cudaEventDestroy(h->done);
+  if (h->wmem) cudaFree(h->wmem);
+  if (h->ws) cudaFree(h->ws);
+  delete h;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* strata_status_str(strata_status s) {
+  switch (s) {
+    case STRATA_OK: return "ok";
+    case STRATA_EINVAL: return "invalid argument";
+    case STRATA_ENOMEM: return "out of device memory";
+    case STRATA_ECUDA: return "CUDA runtime error";
+    case STRATA_EUNSUPPORTED: return "unsupported shape or format";
+    case STRATA_EDEVICE: return "error flagged on the device";
+  }
+  return "unknown status";
+}
+
+strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe_weights* weights, void* cuda_stream,
+                                   strata_window** out) {
+  if (!out) return STRATA_EINVAL;
+  *out = nullptr;
+  strata_status st = check_desc(desc);
+  if (st != STRATA_OK) return st;
+  st = check_weights(desc, weights);
+  if (st != STRATA_OK) return st;
+  if (fault_is("alloc")) return STRATA_ENOMEM;
+
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  strata_window* h = new (std::nothrow) strata_window();
+  if (!h) return STRATA_ENOMEM;
+  h->desc = *desc;
+  const int d = desc->hidden, E = desc->n_experts, k = desc->top_k, F = desc->ffn, Fs = desc->shared_ffn;
+  const int bits = desc->bits, block = desc->block;
+
+  int optin = 0;
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->nsm, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess) {
+    cudaGetLastError();
+    free_handle(h);
+    return STRATA_ECUDA;
+  }
+
+  // ---- kernel-ordered weights + router copy ----
+  const long long pg = packed_bytes(E, F, d, bits), pu = pg, pd = packed_bytes(E, d, F, bits);
+  const long long psg = Fs > 0 ? packed_bytes(1, Fs, d, bits) : 0, psu = psg;
+  const long long psd = Fs > 0 ? packed_bytes(1, d, Fs, bits) : 0;
+  size_t off = 0;
+  const size_t o_gate = off; off = align_up(off + pg, 256);
+  const size_t o_up = off; off = align_up(off + pu, 256);
+  const size_t o_down = off; off = align_up(off + pd, 256);
+  const size_t o_sg = off; off = align_up(off + psg, 256);
+  const size_t o_su = off; off = align_up(off + psu, 256);
+  const size_t o_sd = off; off = align_up(off + psd, 256);
+  const size_t o_rw = off; off = align_up(off + (size_t)E * d * 4, 256);
+  const size_t o_rb = off; off = align_up(off + (size_t)E * 4, 256);
+  h->packed = (long long)off;
+  if (cudaMalloc(&h->wmem, off) != cudaSuccess) {
+    cudaGetLastError();
+    free_handle(h);
+    return STRATA_ENOMEM;
+  }
+  uint8_t* wb = static_cast<uint8_t*>(h->wmem);
+
+  // ---- workspace ----
+  const int nmk_d = (d / block + 15) / 16, nmk_f = (F / block + 15) / 16, nmk_s = Fs > 0 ? (Fs / block + 15) / 16 : 0;
+  size_t w = 0;
+  const size_t o_err = w; w = align_up(w + 8, 256);
+  const size_t o_cnt = w; w = align_up(w + (size_t)(d / 16) * 4, 256);
+  const size_t o_plan = w; w = align_up(w + sizeof(Plan), 256);
+  const size_t o_logit = w; w = align_up(w + (size_t)kMaxRows * E * 4, 256);
+  const size_t o_part = w; w = align_up(w + (size_t)router_partial_floats(d, E) * 4, 256);
+  const size_t o_xf = w; w = align_up(w + (size_t)kMaxRows * frag_halves(d, nmk_d) * 2, 256);
+  const size_t o_hf = w; w = align_up(w + (size_t)kMaxEntries * frag_halves(F, nmk_f) * 2, 256);
+  const size_t o_shf = w; w = align_up(w + (size_t)kMaxRows * (Fs > 0 ? frag_halves(Fs, nmk_s) : 0) * 2, 256);
+  const size_t o_hp = w; w = align_up(w + (size_t)kMaxEntries * (F / 16) * 4, 256);
+  const size_t o_shp = w; w = align_up(w + (size_t)kMaxRows * (Fs / 16) * 4, 256);
+  const size_t o_ob = w; w = align_up(w + (size_t)kMaxEntries * d * 4, 256);
+  const size_t o_sb = w; w = align_up(w + (size_t)kMaxRows * d * 4, 256);
+  h->ws_bytes = (long long)w;
+  if (cudaMalloc(&h->ws, w) != cudaSuccess) {
+    cudaGetLastError();
+    free_handle(h);
+    return STRATA_ENOMEM;
+  }
+  uint8_t* wsb = static_cast<uint8_t*>(h->ws);
+
+  // ---- fill ----
+  cudaError_t e = cudaMemsetAsync(h->ws, 0, w, s);
+  auto rp = [&](const strata_qmat& q, int n, int rows, int K, size_t o) {
+    if (e == cudaSuccess)
+      e = launch_repack(static_cast<const uint8_t*>(q.codes), q.scale, q.min, n, rows, K, bits, wb + o, s);
+  };
+  rp(weights->gate, E, F, d, o_gate);
+  rp(weights->up, E, F, d, o_up);
+  rp(weights->down, E, d, F, o_down);
+  if (Fs > 0) {
+    rp(weights->shared_gate, 1, Fs, d, o_sg);
+    rp(weights->shared_up, 1, Fs, d, o_su);
+    rp(weights->shared_down, 1, d, Fs, o_sd);
+  }
+  if (e == cudaSuccess) e = cudaMemcpyAsync(wb + o_rw, weights->router_w, (size_t)E * d * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && weights->router_b)
+    e = cudaMemcpyAsync(wb + o_rb, weights->router_b, (size_t)E * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->done, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    free_handle(h);
+    return STRATA_ECUDA;
+  }
+
+  LayerDev& L = h->L;
+  L.d = d; L.E = E; L.k = k; L.F = F; L.Fs = Fs; L.bits = bits; L.renorm = desc->renorm_topk;
+  L.router_w = reinterpret_cast<const float*>(wb + o_rw);
+  L.router_b = weights->router_b ? reinterpret_cast<const float*>(wb + o_rb) : nullptr;
+  L.gate = packed_desc(wb + o_gate, F, d, bits);
+  L.up = packed_desc(wb + o_up, F, d, bits);
+  L.down = packed_desc(wb + o_down, d, F, bits);
+  if (Fs > 0) {
+    L.sgate = packed_desc(wb + o_sg, Fs, d, bits);
+    L.sup = packed_desc(wb + o_su, Fs, d, bits);
+    L.sdown = packed_desc(wb + o_sd, d, Fs, bits);
+  } else {
+    L.sgate = L.sup = L.sdown = PackedMat{};
+  }
+
+  WindowBufs& W = h->W;
+  W.err = reinterpret_cast<unsigned*>(wsb + o_err);
+  W.ticket = reinterpret_cast<unsigned*>(wsb + o_err + 4);
+  W.counters = reinterpret_cast<int*>(wsb + o_cnt);
+  W.plan = reinterpret_cast<Plan*>(wsb + o_plan);
+  W.logits = reinterpret_cast<float*>(wsb + o_logit);
+  h->partial = reinterpret_cast<float*>(wsb + o_part);
+  W.xfrag = reinterpret_cast<__half*>(wsb + o_xf);
+  W.hfrag = reinterpret_cast<__half*>(wsb + o_hf);
+  W.shfrag = reinterpret_cast<__half*>(wsb + o_shf);
+  W.hpart = reinterpret_cast<float*>(wsb + o_hp);
+  W.shpart = reinterpret_cast<float*>(wsb + o_shp);
+  W.obuf = reinterpret_cast<float*>(wsb + o_ob);
+  W.sbuf = reinterpret_cast<float*>(wsb + o_sb);
+
+  const int limit = optin - 256;
+  h->c_gateup = expert_smem_cfg(L, 0, desc->max_rows, limit);
+  h->c_down = expert_smem_cfg(L, 1, desc->max_rows, limit);
+  if (h->c_gateup.nstages < 2 || h->c_down.nstages < 2) {
+    free_handle(h);
+    return STRATA_EUNSUPPORTED;
+  }
+  if (expert_set_attrs(bits, 0, h->c_gateup.total_bytes) != cudaSuccess ||
+      expert_set_attrs(bits, 1, h->c_down.total_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    free_handle(h);
+    return STRATA_ECUDA;
+  }
+  *out = h;
+  return STRATA_OK;
+}
+
+strata_status strata_moe_window_forward(strata_window* h, const float* x, int32_t T, float* y,
+                                        const strata_routing_out* routing, void* cuda_stream) {
+  if (!h || !x || !y) return STRATA_EINVAL;
+  if (T < 1 || T > h->desc.max_rows) return STRATA_EINVAL;
+  const size_t bytes = (size_t)T * h->desc.hidden * sizeof(float);
+  const char* xb = reinterpret_cast<const char*>(x);
+  const char* yb = reinterpret_cast<const char*>(y);
+  if (xb < yb + bytes && yb < xb + bytes) return STRATA_EINVAL;
+  if (fault_is("launch")) return STRATA_ECUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+
+  WindowBufs W = h->W;
+  W.x = x;
+  W.y = y;
+  W.T = T;
+  W.out_topk_idx = routing ? routing->topk_idx : nullptr;
+  W.out_topk_w = routing ? routing->topk_w : nullptr;
+  W.out_counts = routing ? routing->counts : nullptr;
+  W.out_offsets = routing ? routing->offsets : nullptr;
+  W.out_entries = routing ? routing->entries : nullptr;
+  W.out_distinct = routing ? routing->distinct : nullptr;
+  W.out_ndistinct = routing ? routing->n_distinct : nullptr;
+
+  launch_router(h->L, W, h->partial, s);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = launch_expert(h->L, W, h->c_gateup, 0, h->nsm, s, true);
+  if (e == cudaSuccess) e = launch_expert(h->L, W, h->c_down, 1, h->nsm, s, true);
+  if (e == cudaSuccess) e = cudaEventRecord(h->done, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return STRATA_ECUDA;
+  }
+  return STRATA_OK;
+}
+
+strata_status strata_window_sync(strata_window* h) {
+  if (!h) return STRATA_EINVAL;
+  if (cudaEventSynchronize(h->done) != cudaSuccess) {
+    cudaGetLastError();
+    return STRATA_ECUDA;
+  }
+  unsigned err = 0;
+  if (cudaMemcpy(&err, h->W.err, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return STRATA_ECUDA;
+  }
+  if (err != 0) {
+    cudaMemset(h->W.err, 0, sizeof(unsigned));
+    return STRATA_EDEVICE;
+  }
+  return STRATA_OK;
+}
+
+strata_status strata_window_query(const strata_window* h, strata_window_info* info) {
+  if (!h || !info) return STRATA_EINVAL;
+  const strata_moe_desc& d = h->desc;
+  info->n_sm = h->nsm;
+  info->stages_gateup = h->c_gateup.nstages;
+  info->stages_down = h->c_down.nstages;
+  info->smem_gateup = h->c_gateup.total_bytes;
+  info->smem_down = h->c_down.total_bytes;
+  info->packed_bytes = h->packed;
+  info->expert_bytes = qmat_bytes(2, d.ffn, d.hidden, d.bits, d.block) + qmat_bytes(1, d.hidden, d.ffn, d.bits, d.block);
+  info->shared_bytes = d.shared_ffn > 0 ? qmat_bytes(2, d.shared_ffn, d.hidden, d.bits, d.block) +
+                                              qmat_bytes(1, d.hidden, d.shared_ffn, d.bits, d.block)
+                                        : 0;
+  info->router_bytes = (long long)d.n_experts * d.hidden * 4 + (h->L.router_b ? d.n_experts * 4 : 0);
+  info->workspace_bytes = h->ws_bytes;
+  return STRATA_OK;
+}
+
+strata_status strata_window_destroy(strata_window* h) {
+  if (!h) return STRATA_OK;
+  free_handle(h);
+  return STRATA_OK;
+}
+
+}  // extern "C"
