@@ -1,0 +1,452 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched verify-window MoE step on GB300.
+
+A step is one window of the ``mid`` workload (d=2048, 128 experts top-8,
+expert width 768, shared expert 768, 4-bit/32 blocks, fp32 router) at T=8
+rows: router, grouping, gate/up, down and combine.  The headline is rows/s
+with inputs resident in HBM and L2 flushed before every timed window; the
+line also carries the T = 1, 2, 4, 8 sweep (rows/s, windows/s, algorithmic
+GB/s), the gate/up kernel's roofline, an end-to-end figure through host
+buffers, the GPU clocks seen, and the fp64 oracle timed on the host cores.
+
+Multi-GPU: the step does not shard (one layer on one GPU); ``--gpus N`` under
+torchrun runs N independent replicas and reports their summed rows over the
+slowest rank's time.
+
+``--impl reference`` times the fp64 oracle (the reference arm of this build)
+on the host cores for the same metric: each step is one row of a T=8 window.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "rows/s per MoE window at T=8 (mid: d2048 E128 top8 F768 +shared768, 4-bit/32)"
+UNIT = "rows/s"
+N_WINDOWS = 64
+SWEEP = (1, 2, 4, 8)
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default="mid")
+    p.add_argument("--rows", type=int, default=8)
+    p.add_argument("--sweep-steps", type=int, default=500)
+    p.add_argument("--cpu-seconds", type=float, default=20.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--mode", choices=("full", "windows"), default="full",
+                   help="windows: only warmup + K windows at --rows (a clean launch sequence for ncu)")
+    return p.parse_args()
+
+
+def workload_desc(wl, T):
+    s = wl.moe
+    return (f"{wl.name}: one MoE layer, d={s.hidden}, {s.n_experts} experts top-{s.top_k}, expert FFN {s.ffn}, "
+            f"shared expert {s.shared_ffn}, {s.bits}-bit blocks of {s.block} (fp16 scale+min), fp32 router, "
+            f"T={T} rows")
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.p = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) != 8:
+                    continue
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+                except ValueError:
+                    continue
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in loaded:
+            for n, v in zip(names, r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "samples_under_load": len(loaded),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------------------------
+# helpers
+
+
+def measured_peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy read+write)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def kernel_source_hash():
+    h = hashlib.sha1()
+    for f in ("experts.cu", "common.cuh", "frag.cuh"):
+        with open(os.path.join(ROOT, "slot_decode_window_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source still matches it."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    try:
+        with open(path) as f:
+            text = f.read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if line.startswith("traffic_bytes_per_launch:") or line.startswith("source_sha1:"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_sha1") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def oracle_rows_per_s(wl, layer_np, xs, budget_s, per_row=True):
+    """Time the fp64 oracle on rows of the windows until the budget is spent."""
+    import oracle
+    done = 0
+    t0 = time.perf_counter()
+    w = 0
+    while True:
+        x = xs[w % len(xs)]
+        for t in range(x.shape[0]):
+            oracle.moe_window(x[t:t + 1], layer_np)
+            done += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        w += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return done / el, done, el
+
+
+# ---------------------------------------------------------------------------------------------
+# reference arm: the oracle
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import numpy as np
+    from slot_decode_window_gb300 import workloads as wlm
+    sys.path.insert(0, ROOT)
+    from tests.helpers import omoe
+    import oracle
+    wl = wlm.WORKLOADS[args.workload]
+    T = args.rows
+    layer = wlm.make_moe_layer(wl.moe, seed=0, cfg_id=wl.cfg_id, device="cpu")
+    ol = omoe(layer)
+    xs = [wlm.make_window(wl, T, seed=0, window=w) for w in range(8)]
+    rows = [(w, t) for w in range(len(xs)) for t in range(T)]
+    for i in range(args.warmup):
+        w, t = rows[i % len(rows)]
+        oracle.moe_window(xs[w][t:t + 1], ol)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        w, t = rows[i % len(rows)]
+        oracle.moe_window(xs[w][t:t + 1], ol)
+    el = time.perf_counter() - t0
+    value = args.steps / el
+    cores = cpu_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(wl, T), "step": "one row of a T-row window, evaluated on its own",
+                   "parallelism": "host cores (numpy BLAS)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} rows cycled over 8 seeded windows of T={T}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
+# our arm
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    from slot_decode_window_gb300 import binding, build, workloads as wlm
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+        build.build()
+    binding.load()
+
+    wl = wlm.WORKLOADS[args.workload]
+    spec = wl.moe
+    d = spec.hidden
+    layer = wlm.make_moe_layer(spec, seed=0, cfg_id=wl.cfg_id, device=str(dev))
+    win = binding.Window(layer, max_rows=8)
+    info = win.info()
+    stream = torch.cuda.current_stream()
+
+    if args.mode == "windows":
+        T = args.rows
+        xw = torch.from_numpy(np.stack([wlm.make_window(wl, T, seed=0, window=w) for w in range(N_WINDOWS)])).to(dev)
+        yw = torch.empty(T, d, device=dev)
+        for i in range(args.warmup + args.steps):
+            win.forward(xw[i % N_WINDOWS], yw)
+        win.sync()
+        if rank == 0:
+            print(json.dumps({"mode": "windows", "workload": args.workload, "T": T, "windows": args.steps}), flush=True)
+        win.close()
+        return
+
+    Ts = sorted(set(SWEEP) | {args.rows})
+    X = {T: torch.from_numpy(np.stack([wlm.make_window(wl, T, seed=0, window=1000 * T + w)
+                                       for w in range(N_WINDOWS)])).to(dev) for T in Ts}
+    Y = torch.empty(8, d, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    # distinct experts of every input window (from the library's own routing output)
+    nd = {}
+    for T in Ts:
+        nd[T] = []
+        for w in range(N_WINDOWS):
+            _, rt = win.forward(X[T][w], Y[:T], routing=True)
+            nd[T].append(int(rt["n_distinct"].item()))
+    win.sync()
+
+    eb, sb, rb = info.expert_bytes, info.shared_bytes, info.router_bytes
+    gu_frac = 2.0 / 3.0  # gate+up are two of an expert's three equal-size matrices
+
+    def window_bytes(T, w):
+        return nd[T][w] * eb + sb + rb + 2 * T * d * 4
+
+    def gateup_bytes(T, w):
+        return (nd[T][w] * eb + sb) * gu_frac + T * d * 4
+
+    def timed(T, steps, warmup):
+        for i in range(warmup):
+            win.forward(X[T][i % N_WINDOWS], Y[:T])
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        t0 = time.perf_counter()
+        for i in range(steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            win.forward(X[T][i % N_WINDOWS], Y[:T])
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        if world > 1:
+            torch.distributed.barrier()
+        ms = [a.elapsed_time(b) for a, b in evs]
+        nbytes = sum(window_bytes(T, i % N_WINDOWS) for i in range(steps))
+        return ms, nbytes, wall
+
+    def reduce_max(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else str(gpu_id or local_rank)
+    sampler = ClockSampler(gpu_id)
+
+    # headline
+    T = args.rows
+    ms, nbytes, wall = timed(T, args.steps, max(3, args.warmup))
+    total_s = reduce_max(sum(ms) / 1e3)
+    rows_total = args.steps * T * world
+    value = rows_total / total_s
+
+    # sweep
+    sweep = {}
+    for Ts_ in SWEEP:
+        m, b, _ = timed(Ts_, args.sweep_steps, 10)
+        tot = sum(m) / 1e3
+        sweep[str(Ts_)] = {"rows_per_s": args.sweep_steps * Ts_ / tot, "windows_per_s": args.sweep_steps / tot,
+                           "us_per_window_median": 1e3 * statistics.median(m),
+                           "algorithmic_GBps": b / tot / 1e9,
+                           "mean_distinct_experts": sum(nd[Ts_]) / len(nd[Ts_])}
+
+    # gate/up kernel roofline: events around each kernel (profiling mode)
+    win.set_profiling(True)
+    prof_steps = min(args.steps, 400)
+    k_ms = [[], [], []]
+    gb = 0.0
+    for i in range(prof_steps):
+        flush.zero_()
+        win.forward(X[T][i % N_WINDOWS], Y[:T])
+        t3 = win.timings()
+        for j in range(3):
+            k_ms[j].append(t3[j])
+        gb += gateup_bytes(T, i % N_WINDOWS)
+    win.set_profiling(False)
+    gu_s = sum(k_ms[1]) / 1e3
+    peak, peak_src = measured_peak_hbm()
+    achieved = gb / gu_s / 1e9
+    traffic = profiled_traffic("expert_gateup", args.workload)
+    roofline = {"kernel": "expert_kernel<4,0> (gate/up + SwiGLU)", "bound": "hbm", "achieved": achieved,
+                "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
+                "traffic": traffic, "algorithmic_bytes_per_launch": gb / prof_steps,
+                "kernel_ms_mean": {"router": statistics.mean(k_ms[0]), "gateup": statistics.mean(k_ms[1]),
+                                   "down_combine": statistics.mean(k_ms[2])},
+                "window_frac_of_peak": (nbytes / (sum(ms) / 1e3) / 1e9) / peak}
+
+    # end to end through host buffers
+    xh = torch.empty(N_WINDOWS, T, d, dtype=torch.float32).pin_memory()
+    xh.copy_(X[T].cpu())
+    yh = torch.empty(T, d, dtype=torch.float32).pin_memory()
+    xd = torch.empty(T, d, device=dev)
+    e2e_steps = min(args.steps, 1000)
+    for i in range(5):
+        xd.copy_(xh[i], non_blocking=True)
+        win.forward(xd, Y[:T])
+        yh.copy_(Y[:T], non_blocking=True)
+    torch.cuda.synchronize()
+    evs = []
+    for i in range(e2e_steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        xd.copy_(xh[i % N_WINDOWS], non_blocking=True)
+        win.forward(xd, Y[:T])
+        yh.copy_(Y[:T], non_blocking=True)
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    e2e_s = reduce_max(sum(a.elapsed_time(b) for a, b in evs) / 1e3)
+    e2e = {"value": e2e_steps * T * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": T * d * 4,
+           "d2h_bytes_per_step": T * d * 4}
+
+    clocks = sampler.stop()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from tests.helpers import omoe
+        ol = omoe(layer)
+        xs = [X[T][w].cpu().numpy() for w in range(4)]
+        rps, done, el = oracle_rows_per_s(wl, ol, xs, args.cpu_seconds)
+        cpu = {"value": rps, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"{done} rows of T={T} windows, each evaluated on its own by the fp64 oracle, {el:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": workload_desc(wl, T), "T": T, "windows": N_WINDOWS,
+                       "l2": "flushed before every timed window (memset of 2x L2 outside the events)",
+                       "parallelism": "replicas only" if world > 1 else "1 GPU",
+                       "arith": "codes -> exact fp16 integers; mma.sync f16 x (fp16 hi + lo activations), fp32 "
+                                "accumulate; fp32 router, softmax, SwiGLU, combine"},
+            "roofline": roofline, "sweep": sweep, "e2e": e2e, "clocks": clocks, "cpu_baseline": cpu,
+            "gpu_launches": 3 * args.steps,
+            "window_us_median": 1e3 * statistics.median(ms), "wall_s_timed_region": wall,
+            "handle": {"n_sm": info.n_sm, "stages_gateup": info.stages_gateup, "stages_down": info.stages_down,
+                       "smem_gateup": info.smem_gateup, "smem_down": info.smem_down},
+        }
+        print(json.dumps(line), flush=True)
+    win.close()
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)  # rank 0 only; the other ranks exit at once
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

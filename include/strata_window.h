@@ -141,6 +141,17 @@ strata_status strata_window_sync(strata_window* h);
 /* Fill *info with the sizes the handle chose. */
 strata_status strata_window_query(const strata_window* h, strata_window_info* info);
 
+/* Measurement aid.  With enable != 0 every later forward call also records
+ * CUDA events on its stream before and after each of its three kernels
+ * (router, gate/up, down+combine); this serialises the kernels, so windows run
+ * a little slower than without it.  enable = 0 turns it off. */
+strata_status strata_window_set_profiling(strata_window* h, int32_t enable);
+
+/* Per-kernel device times (ms) of the last profiled forward call:
+ * ms[0] router, ms[1] gate/up, ms[2] down + combine.  Waits for that call.
+ * Returns EINVAL if profiling was never enabled. */
+strata_status strata_window_timings(strata_window* h, float ms[3]);
+
 /* Free the handle and everything it owns.  NULL is accepted (returns OK). */
 strata_status strata_window_destroy(strata_window* h);
 

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(PKG, "libstrata_window.so")
 STRATA_OK, STRATA_EINVAL, STRATA_ENOMEM, STRATA_ECUDA, STRATA_EUNSUPPORTED, STRATA_EDEVICE = range(6)
 
 EXPORTED = ("strata_window_create", "strata_moe_window_forward", "strata_window_sync", "strata_window_query",
-            "strata_window_destroy", "strata_status_str")
+            "strata_window_set_profiling", "strata_window_timings", "strata_window_destroy", "strata_status_str")
 
 
 class StrataError(RuntimeError):
@@ -80,6 +80,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.strata_window_sync.restype = ctypes.c_int
     lib.strata_window_query.argtypes = [ctypes.c_void_p, P(strata_window_info)]
     lib.strata_window_query.restype = ctypes.c_int
+    lib.strata_window_set_profiling.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+    lib.strata_window_set_profiling.restype = ctypes.c_int
+    lib.strata_window_timings.argtypes = [ctypes.c_void_p, P(ctypes.c_float)]
+    lib.strata_window_timings.restype = ctypes.c_int
     lib.strata_window_destroy.argtypes = [ctypes.c_void_p]
     lib.strata_window_destroy.restype = ctypes.c_int
     lib.strata_status_str.argtypes = [ctypes.c_int]
@@ -119,6 +123,17 @@ def strata_window_query(handle):
     info = strata_window_info()
     st = load().strata_window_query(ctypes.c_void_p(handle), ctypes.byref(info))
     return st, info
+
+
+def strata_window_set_profiling(handle, enable: bool) -> int:
+    return load().strata_window_set_profiling(ctypes.c_void_p(handle), 1 if enable else 0)
+
+
+def strata_window_timings(handle):
+    """Returns (status, [router_ms, gateup_ms, down_ms])."""
+    ms = (ctypes.c_float * 3)()
+    st = load().strata_window_timings(ctypes.c_void_p(handle), ms)
+    return st, list(ms)
 
 
 def strata_window_destroy(handle) -> int:
@@ -195,6 +210,14 @@ class Window:
         check(strata_moe_window_forward(self.handle, x.data_ptr(), T, y.data_ptr(), r, s),
               "strata_moe_window_forward")
         return (y, rt) if routing else y
+
+    def set_profiling(self, enable: bool) -> None:
+        check(strata_window_set_profiling(self.handle, enable), "strata_window_set_profiling")
+
+    def timings(self):
+        st, ms = strata_window_timings(self.handle)
+        check(st, "strata_window_timings")
+        return ms
 
     def sync(self) -> None:
         check(strata_window_sync(self.handle), "strata_window_sync")

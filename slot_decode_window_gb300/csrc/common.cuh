@@ -13,7 +13,7 @@ constexpr int kMaxRows = 8;       // a verify window holds at most 8 rows
 constexpr int kMaxTopK = 8;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxEntries = kMaxRows * kMaxTopK;
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kExpertThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kRouterThreads = 256;
 constexpr int kMaxStages = 8;
@@ -41,7 +41,7 @@ enum : uint32_t {
 //     g, g+8 for blocks 2c, 2c+1, 2c+8, 2c+9 in mma A-fragment order (fp16,
 //     blocks past the end are zero).
 // Code words: each 32-bit word holds pairs of codes at bits (p, p+16) so that
-// one lop3 against 0x64006400 yields an fp16x2 of (1024 + f*q) values.
+// one AND yields an fp16x2 of subnormals f*q*2^-24 (see dq_pair).
 //   4-bit word (one row, one block, lane c covers elements 8c..8c+7):
 //     bits 0/16: e0,e1   4/20: e2,e3 (x16)   8/24: e4,e5   12/28: e6,e7 (x16)
 //   2-bit word (rows g and g+8, two blocks b0,b1, lane c covers elements 4c..4c+3):
@@ -106,24 +106,27 @@ struct WindowBufs {
   float* logits;           // [kMaxRows][E]
   Plan* plan;
   __half* xfrag;           // [kMaxRows][frag(d)]
-  __half* hfrag;           // [kMaxEntries][frag(F)]
-  __half* shfrag;          // [kMaxRows][frag(Fs)]
-  float* hpart;            // [kMaxEntries][F/16]
-  float* shpart;           // [kMaxRows][Fs/16]
+  float2* gu;              // [kMaxEntries][F]: (Wg h, Wu h) of each routed entry
+  float2* sgu;             // [kMaxRows][Fs]: the same for the shared expert
   float* obuf;             // [kMaxEntries][d]
   float* sbuf;             // [kMaxRows][d]
   int* counters;           // [d/16]
-  unsigned* ticket;
+  float* partial;          // router partial logits [njb][kMaxRows][E]
+  int njb;                 // column chunks of the router GEMV
   unsigned* err;
 };
 
 // Shared-memory plan of an expert kernel launch.
 struct SmemCfg {
   int nstages;
-  int stage_bytes;         // max tile bytes of the matrices streamed
+  int stage_bytes;         // one stage: NS sub-tiles' k-chunk (codes+scales, then mins)
+  int sub_stride;          // bytes per sub-tile inside a stage
+  int mins_off;            // offset of the mins part inside a sub-tile slot
+  int nchunks;             // k-chunks per tile
   int bmain_halves;        // B main halves per set: nks_max*8*4*S
   int bsum_halves;         // B sums halves per set: nmk_max*8*4*4
   int nsets;               // 1 (rows <= 4) or 2
+  int max_sub;             // most sub-tiles a task may hold (stage sizing)
   int total_bytes;
 };
 
@@ -149,14 +152,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// The waiting thread may be suspended (up to ~0.1 ms per call) instead of
+// spinning, so waiting warps leave the issue slots to the working ones.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(100000u)
       : "memory");
   return ok != 0;
 }
@@ -197,10 +202,12 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
-// (1024 + f*q) pair -> exact f*q pair in fp16.
-__device__ __forceinline__ uint32_t dq_pair(uint32_t w, uint32_t mask) {
-  return hsub2_u32(lop3_and_or(w, mask, 0x64006400u), 0x64006400u);
-}
+// Two codes at bits (p, p+16) -> an fp16x2 of exact subnormals f*q*2^-24
+// (exponent field zero, the code in the low mantissa bits).  The tensor cores
+// take fp16 subnormal operands exactly, so one AND dequantizes a pair; the
+// 2^-24 is undone once per output.
+__device__ __forceinline__ uint32_t dq_pair(uint32_t w, uint32_t mask) { return w & mask; }
+constexpr float kDqUnscale = 16777216.0f;  // 2^24
 
 // D = A * B + C, m16n8k16, fp16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,

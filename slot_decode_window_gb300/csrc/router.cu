@@ -12,10 +12,10 @@
 // Work split: CTA (eb, jb) computes partial logits of experts [8eb, 8eb+8)
 // over columns [256jb, 256jb+256) with one warp per expert, x's column chunk
 // staged in shared memory.  Every CTA also converts part of x into the
-// activation fragment layout the expert kernels read.  The CTA that arrives
-// last (one atomic ticket, no spinning) sums the partials in a fixed order,
-// runs softmax/top-k per row, and groups the window's entries t*k+j by
-// expert with a counting sort (bit-exact, no atomics).
+// activation fragment layout the expert kernels read (block sums by warp
+// shuffles).  The partial logits are summed in a fixed order, and the
+// softmax, top-k and grouping run, at the start of the gate/up kernel (see
+// experts.cu), so this kernel has no serial tail.
 #include "common.cuh"
 #include "frag.cuh"
 #include "kernels.h"
@@ -27,55 +27,50 @@ constexpr int kRouterExpertsPerCta = 8;
 
 template <int BITS>
 __device__ void write_x_frags(const LayerDev& L, const WindowBufs& W) {
+  constexpr int B = Fmt<BITS>::kBlock;
   const int d = L.d;
-  const int nblk = d / Fmt<BITS>::kBlock;
-  const int nmk = (nblk + 15) / 16;
+  const int nmk = (d / B + 15) / 16;
   const long long fh = frag_halves(d, nmk);
-  const long long n_el = (long long)W.T * d;
-  const long long n_sum = (long long)W.T * nmk * 16;
+  const long long n_el = (long long)W.T * d;  // a multiple of 64: warps never straddle a block or a row
   const long long stride = (long long)gridDim.x * gridDim.y * blockDim.x;
   const long long tid = ((long long)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
-  for (long long i = tid; i < n_el; i += stride) {
-    const int t = (int)(i / d), j = (int)(i % d);
-    const float v = W.x[i];
-    int off;
-    float f;
-    frag_main_pos<BITS>(j, off, f);
-    __half hi, lo;
-    split_hi_lo(v * f, hi, lo);
+  const long long n_iter = (n_el + stride - 1) / stride;
+  for (long long it = 0; it < n_iter; ++it) {
+    const long long i = tid + it * stride;
+    const bool in = i < n_el;
+    const int t = in ? (int)(i / d) : 0, j = in ? (int)(i % d) : 0;
+    const float v = in ? W.x[i] : 0.f;
     __half* base = W.xfrag + t * fh;
-    base[off] = hi;
-    base[d + off] = lo;
-  }
-  for (long long i = tid; i < n_sum; i += stride) {
-    const int t = (int)(i / (nmk * 16)), beta = (int)(i % (nmk * 16));
-    float s = 0.f;
-    if (beta < nblk) {
-      const float* xr = W.x + (long long)t * d + beta * Fmt<BITS>::kBlock;
-      for (int e = 0; e < Fmt<BITS>::kBlock; ++e) s += xr[e];
+    if (in) {
+      int off;
+      float f;
+      frag_main_pos<BITS>(j, off, f);
+      __half hi, lo;
+      split_hi_lo(v * f, hi, lo);
+      base[off] = hi;
+      base[d + off] = lo;
     }
-    __half hi, lo;
-    split_hi_lo(s, hi, lo);
-    __half* base = W.xfrag + t * fh + 2 * d;
-    const int off = frag_sum_pos(beta);
-    base[off] = hi;
-    base[nmk * 16 + off] = lo;
+    float s = v;
+#pragma unroll
+    for (int o = B / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (in && (j % B) == 0) {
+      __half hi, lo;
+      split_hi_lo(s, hi, lo);
+      const int off = frag_sum_pos(j / B);
+      base[2 * d + off] = hi;
+      base[2 * d + nmk * 16 + off] = lo;
+    }
   }
 }
 
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(LayerDev L, WindowBufs W, float* partial) {
   __shared__ __align__(16) float xs[kMaxRows][kRouterCols];
-  __shared__ float lg[kMaxRows][kMaxExperts];
-  __shared__ int sel[kMaxEntries];
-  __shared__ int cnt[kMaxExperts];
-  __shared__ int flag[kMaxExperts];
-  __shared__ int is_last;
 
   // The expert kernel may start its prologue now; it waits for this grid's
   // completion before reading anything written here.
   griddep_launch_dependents();
 
-  const int T = W.T, d = L.d, E = L.E, k = L.k;
+  const int T = W.T, d = L.d, E = L.E;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int jb = blockIdx.y;
   const int j0 = jb * kRouterCols;
@@ -123,119 +118,6 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(LayerDev L, Wind
     for (int i = tid; i < d / 16; i += blockDim.x) W.counters[i] = 0;
   }
 
-  // -- last CTA: softmax, top-k, grouping -----------------------------------
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned total = gridDim.x * gridDim.y;
-    is_last = (atomicAdd(W.ticket, 1u) == total - 1u);
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-
-  const int njb = gridDim.y;
-  for (int i = tid; i < T * E; i += blockDim.x) {
-    const int t = i / E, e = i % E;
-    float v = 0.f;
-    for (int b = 0; b < njb; ++b) v += __ldcg(partial + ((long long)b * kMaxRows + t) * E + e);
-    if (L.router_b) v += L.router_b[e];
-    lg[t][e] = v;
-    W.logits[t * E + e] = v;
-  }
-  __syncthreads();
-
-  Plan* P = W.plan;
-  if (warp < T) {
-    const int t = warp;
-    float m = -INFINITY;
-    bool finite = true;
-    for (int e = lane; e < E; e += 32) {
-      const float v = lg[t][e];
-      finite &= isfinite(v);
-      m = fmaxf(m, v);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (!__all_sync(0xffffffffu, finite) && lane == 0) atomicOr(W.err, kErrNonFinite);
-    float z = 0.f;
-    for (int e = lane; e < E; e += 32) z += expf(lg[t][e] - m);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    // top-k by logit, descending, ties -> lower expert index
-    unsigned taken = 0u;  // bit i: expert lane + 32*i already selected
-    float wsum = 0.f;
-    float wsel[kMaxTopK];
-    int esel[kMaxTopK];
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-      for (int i = 0, e = lane; e < E; ++i, e += 32) {
-        const float v = lg[t][e];
-        if (!((taken >> i) & 1u) && (v > bv || (v == bv && e < be))) { bv = v; be = e; }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-      }
-      if (be == 0x7fffffff) be = 0;  // only with non-finite logits
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      esel[j] = be;
-      wsel[j] = expf(bv - m) / z;
-      wsum += wsel[j];
-    }
-    if (lane == 0) {
-      for (int j = 0; j < k; ++j) {
-        const float g = L.renorm ? wsel[j] / wsum : wsel[j];
-        sel[t * k + j] = esel[j];
-        P->topk_idx[t * k + j] = esel[j];
-        P->topk_w[t * k + j] = g;
-        if (W.out_topk_idx) W.out_topk_idx[t * k + j] = esel[j];
-        if (W.out_topk_w) W.out_topk_w[t * k + j] = g;
-      }
-    }
-  }
-  __syncthreads();
-
-  // counting sort of entries by expert
-  const int nent = T * k;
-  for (int e = tid; e < E; e += blockDim.x) {
-    int c = 0;
-    for (int i = 0; i < nent; ++i) c += (sel[i] == e);
-    cnt[e] = c;
-    flag[e] = c > 0;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int off = 0, nd = 0;
-    for (int e = 0; e < E; ++e) {
-      P->offsets[e] = off;
-      if (W.out_offsets) W.out_offsets[e] = off;
-      off += cnt[e];
-      if (flag[e]) { P->distinct[nd] = e; if (W.out_distinct) W.out_distinct[nd] = e; ++nd; }
-    }
-    P->offsets[E] = off;
-    if (W.out_offsets) W.out_offsets[E] = off;
-    P->n_distinct = nd;
-    P->T = T;
-    if (W.out_ndistinct) *W.out_ndistinct = nd;
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
-    P->counts[e] = cnt[e];
-    if (W.out_counts) W.out_counts[e] = cnt[e];
-    int pos = P->offsets[e];
-    for (int i = 0; i < nent; ++i) {
-      if (sel[i] == e) {
-        P->entries[pos] = i;
-        if (W.out_entries) W.out_entries[pos] = i;
-        ++pos;
-      }
-    }
-  }
-  if (tid == 0) *W.ticket = 0u;
 }
 
 void launch_router(const LayerDev& L, const WindowBufs& W, float* partial, cudaStream_t s) {

@@ -24,6 +24,9 @@ struct strata_window {
   void* ws = nullptr;
   long long packed = 0, ws_bytes = 0;
   cudaEvent_t done = nullptr;
+  bool profiling = false;
+  bool profiled_once = false;
+  cudaEvent_t prof[4] = {nullptr, nullptr, nullptr, nullptr};
 };
 
 namespace {
@@ -70,6 +73,8 @@ long long qmat_bytes(int n, int rows, int cols, int bits, int block) {
 void free_handle(strata_window* h) {
   if (!h) return;
   if (h->done) cudaEventDestroy(h->done);
+  for (cudaEvent_t& ev : h->prof)
+    if (ev) cudaEventDestroy(ev);
   if (h->wmem) cudaFree(h->wmem);
   if (h->ws) cudaFree(h->ws);
   delete h;
@@ -139,7 +144,7 @@ strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe
   uint8_t* wb = static_cast<uint8_t*>(h->wmem);
 
   // ---- workspace ----
-  const int nmk_d = (d / block + 15) / 16, nmk_f = (F / block + 15) / 16, nmk_s = Fs > 0 ? (Fs / block + 15) / 16 : 0;
+  const int nmk_d = (d / block + 15) / 16;
   size_t w = 0;
   const size_t o_err = w; w = align_up(w + 8, 256);
   const size_t o_cnt = w; w = align_up(w + (size_t)(d / 16) * 4, 256);
@@ -147,10 +152,8 @@ strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe
   const size_t o_logit = w; w = align_up(w + (size_t)kMaxRows * E * 4, 256);
   const size_t o_part = w; w = align_up(w + (size_t)router_partial_floats(d, E) * 4, 256);
   const size_t o_xf = w; w = align_up(w + (size_t)kMaxRows * frag_halves(d, nmk_d) * 2, 256);
-  const size_t o_hf = w; w = align_up(w + (size_t)kMaxEntries * frag_halves(F, nmk_f) * 2, 256);
-  const size_t o_shf = w; w = align_up(w + (size_t)kMaxRows * (Fs > 0 ? frag_halves(Fs, nmk_s) : 0) * 2, 256);
-  const size_t o_hp = w; w = align_up(w + (size_t)kMaxEntries * (F / 16) * 4, 256);
-  const size_t o_shp = w; w = align_up(w + (size_t)kMaxRows * (Fs / 16) * 4, 256);
+  const size_t o_gu = w; w = align_up(w + (size_t)kMaxEntries * F * 8, 256);
+  const size_t o_sgu = w; w = align_up(w + (size_t)kMaxRows * Fs * 8, 256);
   const size_t o_ob = w; w = align_up(w + (size_t)kMaxEntries * d * 4, 256);
   const size_t o_sb = w; w = align_up(w + (size_t)kMaxRows * d * 4, 256);
   h->ws_bytes = (long long)w;
@@ -203,20 +206,19 @@ strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe
 
   WindowBufs& W = h->W;
   W.err = reinterpret_cast<unsigned*>(wsb + o_err);
-  W.ticket = reinterpret_cast<unsigned*>(wsb + o_err + 4);
   W.counters = reinterpret_cast<int*>(wsb + o_cnt);
   W.plan = reinterpret_cast<Plan*>(wsb + o_plan);
   W.logits = reinterpret_cast<float*>(wsb + o_logit);
   h->partial = reinterpret_cast<float*>(wsb + o_part);
+  W.partial = h->partial;
+  W.njb = router_partial_floats(d, E) / (kMaxRows * E);
   W.xfrag = reinterpret_cast<__half*>(wsb + o_xf);
-  W.hfrag = reinterpret_cast<__half*>(wsb + o_hf);
-  W.shfrag = reinterpret_cast<__half*>(wsb + o_shf);
-  W.hpart = reinterpret_cast<float*>(wsb + o_hp);
-  W.shpart = reinterpret_cast<float*>(wsb + o_shp);
+  W.gu = reinterpret_cast<float2*>(wsb + o_gu);
+  W.sgu = reinterpret_cast<float2*>(wsb + o_sgu);
   W.obuf = reinterpret_cast<float*>(wsb + o_ob);
   W.sbuf = reinterpret_cast<float*>(wsb + o_sb);
 
-  const int limit = optin - 256;
+  const int limit = optin - 8192;  // leave room for the kernels' static shared memory
   h->c_gateup = expert_smem_cfg(L, 0, desc->max_rows, limit);
   h->c_down = expert_smem_cfg(L, 1, desc->max_rows, limit);
   if (h->c_gateup.nstages < 2 || h->c_down.nstages < 2) {
@@ -256,11 +258,19 @@ strata_status strata_moe_window_forward(strata_window* h, const float* x, int32_
   W.out_distinct = routing ? routing->distinct : nullptr;
   W.out_ndistinct = routing ? routing->n_distinct : nullptr;
 
-  launch_router(h->L, W, h->partial, s);
-  cudaError_t e = cudaGetLastError();
+  const bool prof = h->profiling;
+  cudaError_t e = prof ? cudaEventRecord(h->prof[0], s) : cudaSuccess;
+  if (e == cudaSuccess) {
+    launch_router(h->L, W, h->partial, s);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess && prof) e = cudaEventRecord(h->prof[1], s);
   if (e == cudaSuccess) e = launch_expert(h->L, W, h->c_gateup, 0, h->nsm, s, true);
+  if (e == cudaSuccess && prof) e = cudaEventRecord(h->prof[2], s);
   if (e == cudaSuccess) e = launch_expert(h->L, W, h->c_down, 1, h->nsm, s, true);
+  if (e == cudaSuccess && prof) e = cudaEventRecord(h->prof[3], s);
   if (e == cudaSuccess) e = cudaEventRecord(h->done, s);
+  if (e == cudaSuccess && prof) h->profiled_once = true;
   if (e != cudaSuccess) {
     cudaGetLastError();
     return STRATA_ECUDA;
@@ -301,6 +311,35 @@ strata_status strata_window_query(const strata_window* h, strata_window_info* in
                                         : 0;
   info->router_bytes = (long long)d.n_experts * d.hidden * 4 + (h->L.router_b ? d.n_experts * 4 : 0);
   info->workspace_bytes = h->ws_bytes;
+  return STRATA_OK;
+}
+
+strata_status strata_window_set_profiling(strata_window* h, int32_t enable) {
+  if (!h) return STRATA_EINVAL;
+  if (enable && !h->prof[0]) {
+    for (cudaEvent_t& ev : h->prof) {
+      if (cudaEventCreate(&ev) != cudaSuccess) {
+        cudaGetLastError();
+        return STRATA_ECUDA;
+      }
+    }
+  }
+  h->profiling = enable != 0;
+  return STRATA_OK;
+}
+
+strata_status strata_window_timings(strata_window* h, float ms[3]) {
+  if (!h || !ms || !h->profiled_once) return STRATA_EINVAL;
+  if (cudaEventSynchronize(h->prof[3]) != cudaSuccess) {
+    cudaGetLastError();
+    return STRATA_ECUDA;
+  }
+  for (int i = 0; i < 3; ++i) {
+    if (cudaEventElapsedTime(&ms[i], h->prof[i], h->prof[i + 1]) != cudaSuccess) {
+      cudaGetLastError();
+      return STRATA_ECUDA;
+    }
+  }
   return STRATA_OK;
 }
 
