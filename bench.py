@@ -131,7 +131,7 @@ def measured_peak_hbm():
 
 def kernel_source_hash():
     h = hashlib.sha1()
-    for f in ("experts.cu", "common.cuh", "frag.cuh"):
+    for f in ("window.cu", "common.cuh", "frag.cuh"):
         with open(os.path.join(ROOT, "slot_decode_window_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
@@ -288,13 +288,9 @@ def run_ours(args, rank, world, local_rank):
     win.sync()
 
     eb, sb, rb = info.expert_bytes, info.shared_bytes, info.router_bytes
-    gu_frac = 2.0 / 3.0  # gate+up are two of an expert's three equal-size matrices
 
     def window_bytes(T, w):
         return nd[T][w] * eb + sb + rb + 2 * T * d * 4
-
-    def gateup_bytes(T, w):
-        return (nd[T][w] * eb + sb) * gu_frac + T * d * 4
 
     def timed(T, steps, warmup):
         for i in range(warmup):
@@ -345,29 +341,25 @@ def run_ours(args, rank, world, local_rank):
                            "algorithmic_GBps": b / tot / 1e9,
                            "mean_distinct_experts": sum(nd[Ts_]) / len(nd[Ts_])}
 
-    # gate/up kernel roofline: events around each kernel (profiling mode)
+    # window kernel roofline: events right around the kernel (profiling mode)
     win.set_profiling(True)
     prof_steps = min(args.steps, 400)
-    k_ms = [[], [], []]
-    gb = 0.0
+    k_ms = []
+    wb = 0.0
     for i in range(prof_steps):
         flush.zero_()
         win.forward(X[T][i % N_WINDOWS], Y[:T])
-        t3 = win.timings()
-        for j in range(3):
-            k_ms[j].append(t3[j])
-        gb += gateup_bytes(T, i % N_WINDOWS)
+        k_ms.append(win.timings())
+        wb += window_bytes(T, i % N_WINDOWS)
     win.set_profiling(False)
-    gu_s = sum(k_ms[1]) / 1e3
+    k_s = sum(k_ms) / 1e3
     peak, peak_src = measured_peak_hbm()
-    achieved = gb / gu_s / 1e9
-    traffic = profiled_traffic("expert_gateup", args.workload)
-    roofline = {"kernel": "expert_kernel<4,0> (gate/up + SwiGLU)", "bound": "hbm", "achieved": achieved,
-                "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
-                "traffic": traffic, "algorithmic_bytes_per_launch": gb / prof_steps,
-                "kernel_ms_mean": {"router": statistics.mean(k_ms[0]), "gateup": statistics.mean(k_ms[1]),
-                                   "down_combine": statistics.mean(k_ms[2])},
-                "window_frac_of_peak": (nbytes / (sum(ms) / 1e3) / 1e9) / peak}
+    achieved = wb / k_s / 1e9
+    traffic = profiled_traffic("window_kernel", args.workload)
+    roofline = {"kernel": "window_kernel<4> (router, grouping, gate/up, down, combine)", "bound": "hbm",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
+                "traffic": traffic, "algorithmic_bytes_per_launch": wb / prof_steps,
+                "kernel_us_mean": 1e3 * statistics.mean(k_ms), "kernel_us_median": 1e3 * statistics.median(k_ms)}
 
     # end to end through host buffers
     xh = torch.empty(N_WINDOWS, T, d, dtype=torch.float32).pin_memory()
@@ -417,10 +409,10 @@ def run_ours(args, rank, world, local_rank):
                        "arith": "codes -> exact fp16 integers; mma.sync f16 x (fp16 hi + lo activations), fp32 "
                                 "accumulate; fp32 router, softmax, SwiGLU, combine"},
             "roofline": roofline, "sweep": sweep, "e2e": e2e, "clocks": clocks, "cpu_baseline": cpu,
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": args.steps,
             "window_us_median": 1e3 * statistics.median(ms), "wall_s_timed_region": wall,
-            "handle": {"n_sm": info.n_sm, "stages_gateup": info.stages_gateup, "stages_down": info.stages_down,
-                       "smem_gateup": info.smem_gateup, "smem_down": info.smem_down},
+            "handle": {"n_sm": info.n_sm, "stages": info.stages, "stage_bytes": info.stage_bytes,
+                       "smem_bytes": info.smem_bytes},
         }
         print(json.dumps(line), flush=True)
     win.close()

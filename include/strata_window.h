@@ -103,11 +103,10 @@ typedef struct {
 
 /* Sizes a handle chose (for measurement and tests). */
 typedef struct {
-  int32_t n_sm;               /* SMs of the device (grid of the expert kernels) */
-  int32_t stages_gateup;      /* shared-memory ring stages of the gate/up kernel */
-  int32_t stages_down;        /* ... of the down kernel */
-  int32_t smem_gateup;        /* dynamic shared memory bytes per CTA */
-  int32_t smem_down;
+  int32_t n_sm;               /* SMs of the device (CTAs of the window kernel) */
+  int32_t stages;             /* shared-memory ring stages of the window kernel */
+  int32_t stage_bytes;        /* bytes per ring stage */
+  int32_t smem_bytes;         /* dynamic shared memory bytes per CTA */
   int64_t packed_bytes;       /* bytes of the handle's kernel-ordered weights */
   int64_t expert_bytes;       /* block-format bytes of one routed expert (gate+up+down) */
   int64_t shared_bytes;       /* block-format bytes of the shared expert */
@@ -126,7 +125,7 @@ strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe
 
 /* Run one window: y = MoE(x) for T rows.
  *   x: device fp32 [T][d], caller-owned; y: device fp32 [T][d], caller-owned,
- *   must not overlap x.  1 <= T <= desc.max_rows.
+ *   must not overlap x; both 16-byte aligned.  1 <= T <= desc.max_rows.
  *   routing: NULL, or a struct of optional device outputs.
  *   cuda_stream: the stream to enqueue on (NULL = default stream).
  * Asynchronous: returns once the work is enqueued.  One handle serves one
@@ -142,15 +141,13 @@ strata_status strata_window_sync(strata_window* h);
 strata_status strata_window_query(const strata_window* h, strata_window_info* info);
 
 /* Measurement aid.  With enable != 0 every later forward call also records
- * CUDA events on its stream before and after each of its three kernels
- * (router, gate/up, down+combine); this serialises the kernels, so windows run
- * a little slower than without it.  enable = 0 turns it off. */
+ * CUDA events on its stream right before and after its window kernel.
+ * enable = 0 turns it off. */
 strata_status strata_window_set_profiling(strata_window* h, int32_t enable);
 
-/* Per-kernel device times (ms) of the last profiled forward call:
- * ms[0] router, ms[1] gate/up, ms[2] down + combine.  Waits for that call.
- * Returns EINVAL if profiling was never enabled. */
-strata_status strata_window_timings(strata_window* h, float ms[3]);
+/* Device time (ms) of the window kernel of the last profiled forward call;
+ * waits for that call.  Returns EINVAL if profiling was never enabled. */
+strata_status strata_window_timings(strata_window* h, float* ms);
 
 /* Free the handle and everything it owns.  NULL is accepted (returns OK). */
 strata_status strata_window_destroy(strata_window* h);

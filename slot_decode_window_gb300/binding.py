@@ -51,8 +51,8 @@ class strata_routing_out(ctypes.Structure):
 
 
 class strata_window_info(ctypes.Structure):
-    _fields_ = [("n_sm", ctypes.c_int32), ("stages_gateup", ctypes.c_int32), ("stages_down", ctypes.c_int32),
-                ("smem_gateup", ctypes.c_int32), ("smem_down", ctypes.c_int32), ("packed_bytes", ctypes.c_int64),
+    _fields_ = [("n_sm", ctypes.c_int32), ("stages", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("packed_bytes", ctypes.c_int64),
                 ("expert_bytes", ctypes.c_int64), ("shared_bytes", ctypes.c_int64), ("router_bytes", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64)]
 
@@ -130,10 +130,10 @@ def strata_window_set_profiling(handle, enable: bool) -> int:
 
 
 def strata_window_timings(handle):
-    """Returns (status, [router_ms, gateup_ms, down_ms])."""
-    ms = (ctypes.c_float * 3)()
-    st = load().strata_window_timings(ctypes.c_void_p(handle), ms)
-    return st, list(ms)
+    """Returns (status, window kernel ms)."""
+    ms = ctypes.c_float()
+    st = load().strata_window_timings(ctypes.c_void_p(handle), ctypes.byref(ms))
+    return st, ms.value
 
 
 def strata_window_destroy(handle) -> int:

@@ -76,18 +76,6 @@ struct PackedMat {
 //   sums lo [nmk][4][4].  Size in halves: 2*K + 32*nmk.
 __host__ __device__ inline long long frag_halves(int K, int nmk) { return 2LL * K + 32LL * nmk; }
 
-// Routing plan written by the router kernel's last CTA.
-struct Plan {
-  int n_distinct;
-  int T;
-  int distinct[kMaxExperts];
-  int counts[kMaxExperts];
-  int offsets[kMaxExperts + 1];
-  int entries[kMaxEntries];
-  int topk_idx[kMaxEntries];
-  float topk_w[kMaxEntries];
-};
-
 struct LayerDev {
   int d, E, k, F, Fs, bits, renorm;
   const float* router_w;   // [E][d]
@@ -103,31 +91,40 @@ struct WindowBufs {
   int* out_topk_idx; float* out_topk_w; int* out_counts; int* out_offsets;
   int* out_entries; int* out_distinct; int* out_ndistinct;
   // workspace
-  float* logits;           // [kMaxRows][E]
-  Plan* plan;
   __half* xfrag;           // [kMaxRows][frag(d)]
   float2* gu;              // [kMaxEntries][F]: (Wg h, Wu h) of each routed entry
   float2* sgu;             // [kMaxRows][Fs]: the same for the shared expert
   float* obuf;             // [kMaxEntries][d]
   float* sbuf;             // [kMaxRows][d]
-  int* counters;           // [d/16]
+  int* counters;           // [d/16] contributions landed per 16-row slice of y
+  int* done_gu;            // [E+1] finished gate/up tasks per group (shared first)
+  unsigned long long* gbar;  // grid barrier arrivals (monotonic across windows)
   float* partial;          // router partial logits [njb][kMaxRows][E]
   int njb;                 // column chunks of the router GEMV
   unsigned* err;
 };
 
-// Shared-memory plan of an expert kernel launch.
-struct SmemCfg {
-  int nstages;
-  int stage_bytes;         // one stage: NS sub-tiles' k-chunk (codes+scales, then mins)
+constexpr int kMaxChunks = 32;  // k-chunks per tile
+
+// How one phase (0 gate/up, 1 down) cuts its tiles into ring stages.
+struct PhaseCfg {
+  int nchunks;             // k-chunks per tile
   int sub_stride;          // bytes per sub-tile inside a stage
   int mins_off;            // offset of the mins part inside a sub-tile slot
-  int nchunks;             // k-chunks per tile
-  int bmain_halves;        // B main halves per set: nks_max*8*4*S
+  int max_sub;             // most sub-tiles a task may hold (stage sizing)
+  short cks[2][kMaxChunks + 1];  // k-step bounds of each chunk: [0] routed K, [1] shared K
+  short cmk[2][kMaxChunks + 1];  // min-group bounds of each chunk
+};
+
+// Shared-memory plan of the window kernel.
+struct KernelCfg {
+  int nstages;
+  int stage_bytes;         // one stage: up to max_sub sub-tiles' k-chunk (codes+scales, then mins)
+  int bmain_halves;        // B main halves per set: 8 * max K
   int bsum_halves;         // B sums halves per set: nmk_max*8*4*4
   int nsets;               // 1 (rows <= 4) or 2
-  int max_sub;             // most sub-tiles a task may hold (stage sizing)
   int total_bytes;
+  PhaseCfg ph[2];
 };
 
 // ---------------------------------------------------------------------------

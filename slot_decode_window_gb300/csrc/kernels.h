@@ -4,14 +4,15 @@
 
 namespace strata {
 
-void launch_router(const LayerDev& L, const WindowBufs& W, float* partial, cudaStream_t s);
-int router_partial_floats(int d, int E);
+constexpr int kRouterCols = 256;  // columns per router partial-logit chunk
 
-// Expert phases: 0 = gate/up + SwiGLU (writes h fragments), 1 = down + combine.
-SmemCfg expert_smem_cfg(const LayerDev& L, int phase, int max_rows, int smem_limit);
-cudaError_t expert_set_attrs(int bits, int phase, int smem_bytes);
-cudaError_t launch_expert(const LayerDev& L, const WindowBufs& W, const SmemCfg& C, int phase, int grid,
-                          cudaStream_t s, bool pdl);
+// Shared-memory plan of the window kernel for one layer shape.
+KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit);
+cudaError_t window_set_attrs(int bits, int smem_bytes);
+// CTAs of the window kernel that one SM holds (0 if it does not fit).
+int window_blocks_per_sm(int bits, int smem_bytes);
+// One window: router, grouping, gate/up, down and combine in one cooperative launch.
+cudaError_t launch_window(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, int grid, cudaStream_t s);
 
 // Repack one canonical block-quantized matrix stack into the tile format.
 cudaError_t launch_repack(const uint8_t* codes, const uint16_t* scale, const uint16_t* mn, int n, int rows, int K,

@@ -1,7 +1,6 @@
 // C ABI of the verify-window MoE step: argument checks, the handle's memory
-// (kernel-ordered weights + window workspace), and the per-window launch
-// sequence router -> gate/up -> down+combine (programmatic dependent launch
-// between them).
+// (kernel-ordered weights + window workspace), and the per-window launch of
+// the persistent window kernel (one cooperative launch, one CTA per SM).
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -18,7 +17,7 @@ struct strata_window {
   int nsm = 0;
   LayerDev L{};
   WindowBufs W{};
-  SmemCfg c_gateup{}, c_down{};
+  KernelCfg cfg{};
   float* partial = nullptr;
   void* wmem = nullptr;
   void* ws = nullptr;
@@ -26,7 +25,7 @@ struct strata_window {
   cudaEvent_t done = nullptr;
   bool profiling = false;
   bool profiled_once = false;
-  cudaEvent_t prof[4] = {nullptr, nullptr, nullptr, nullptr};
+  cudaEvent_t prof[2] = {nullptr, nullptr};
 };
 
 namespace {
@@ -146,11 +145,12 @@ strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe
   // ---- workspace ----
   const int nmk_d = (d / block + 15) / 16;
   size_t w = 0;
+  const int njb = (d + kRouterCols - 1) / kRouterCols;
   const size_t o_err = w; w = align_up(w + 8, 256);
+  const size_t o_gbar = w; w = align_up(w + 8, 256);
   const size_t o_cnt = w; w = align_up(w + (size_t)(d / 16) * 4, 256);
-  const size_t o_plan = w; w = align_up(w + sizeof(Plan), 256);
-  const size_t o_logit = w; w = align_up(w + (size_t)kMaxRows * E * 4, 256);
-  const size_t o_part = w; w = align_up(w + (size_t)router_partial_floats(d, E) * 4, 256);
+  const size_t o_done = w; w = align_up(w + (size_t)(E + 1) * 4, 256);
+  const size_t o_part = w; w = align_up(w + (size_t)njb * kMaxRows * E * 4, 256);
   const size_t o_xf = w; w = align_up(w + (size_t)kMaxRows * frag_halves(d, nmk_d) * 2, 256);
   const size_t o_gu = w; w = align_up(w + (size_t)kMaxEntries * F * 8, 256);
   const size_t o_sgu = w; w = align_up(w + (size_t)kMaxRows * Fs * 8, 256);
@@ -206,30 +206,33 @@ strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe
 
   WindowBufs& W = h->W;
   W.err = reinterpret_cast<unsigned*>(wsb + o_err);
+  W.gbar = reinterpret_cast<unsigned long long*>(wsb + o_gbar);
   W.counters = reinterpret_cast<int*>(wsb + o_cnt);
-  W.plan = reinterpret_cast<Plan*>(wsb + o_plan);
-  W.logits = reinterpret_cast<float*>(wsb + o_logit);
+  W.done_gu = reinterpret_cast<int*>(wsb + o_done);
   h->partial = reinterpret_cast<float*>(wsb + o_part);
   W.partial = h->partial;
-  W.njb = router_partial_floats(d, E) / (kMaxRows * E);
+  W.njb = njb;
   W.xfrag = reinterpret_cast<__half*>(wsb + o_xf);
   W.gu = reinterpret_cast<float2*>(wsb + o_gu);
   W.sgu = reinterpret_cast<float2*>(wsb + o_sgu);
   W.obuf = reinterpret_cast<float*>(wsb + o_ob);
   W.sbuf = reinterpret_cast<float*>(wsb + o_sb);
 
-  const int limit = optin - 8192;  // leave room for the kernels' static shared memory
-  h->c_gateup = expert_smem_cfg(L, 0, desc->max_rows, limit);
-  h->c_down = expert_smem_cfg(L, 1, desc->max_rows, limit);
-  if (h->c_gateup.nstages < 2 || h->c_down.nstages < 2) {
+  const int limit = optin - 12288;  // leave room for the kernel's static shared memory
+  h->cfg = window_cfg(L, desc->max_rows, limit);
+  if (h->cfg.nstages < 2) {
     free_handle(h);
     return STRATA_EUNSUPPORTED;
   }
-  if (expert_set_attrs(bits, 0, h->c_gateup.total_bytes) != cudaSuccess ||
-      expert_set_attrs(bits, 1, h->c_down.total_bytes) != cudaSuccess) {
+  if (window_set_attrs(bits, h->cfg.total_bytes) != cudaSuccess) {
     cudaGetLastError();
     free_handle(h);
     return STRATA_ECUDA;
+  }
+  // the window kernel's CTAs wait on one another: all of them must be resident
+  if (window_blocks_per_sm(bits, h->cfg.total_bytes) < 1) {
+    free_handle(h);
+    return STRATA_EUNSUPPORTED;
   }
   *out = h;
   return STRATA_OK;
@@ -243,6 +246,7 @@ strata_status strata_moe_window_forward(strata_window* h, const float* x, int32_
   const char* xb = reinterpret_cast<const char*>(x);
   const char* yb = reinterpret_cast<const char*>(y);
   if (xb < yb + bytes && yb < xb + bytes) return STRATA_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) % 16 != 0) return STRATA_EINVAL;
   if (fault_is("launch")) return STRATA_ECUDA;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
 
@@ -260,15 +264,8 @@ strata_status strata_moe_window_forward(strata_window* h, const float* x, int32_
 
   const bool prof = h->profiling;
   cudaError_t e = prof ? cudaEventRecord(h->prof[0], s) : cudaSuccess;
-  if (e == cudaSuccess) {
-    launch_router(h->L, W, h->partial, s);
-    e = cudaGetLastError();
-  }
+  if (e == cudaSuccess) e = launch_window(h->L, W, h->cfg, h->nsm, s);
   if (e == cudaSuccess && prof) e = cudaEventRecord(h->prof[1], s);
-  if (e == cudaSuccess) e = launch_expert(h->L, W, h->c_gateup, 0, h->nsm, s, true);
-  if (e == cudaSuccess && prof) e = cudaEventRecord(h->prof[2], s);
-  if (e == cudaSuccess) e = launch_expert(h->L, W, h->c_down, 1, h->nsm, s, true);
-  if (e == cudaSuccess && prof) e = cudaEventRecord(h->prof[3], s);
   if (e == cudaSuccess) e = cudaEventRecord(h->done, s);
   if (e == cudaSuccess && prof) h->profiled_once = true;
   if (e != cudaSuccess) {
@@ -300,10 +297,9 @@ strata_status strata_window_query(const strata_window* h, strata_window_info* in
   if (!h || !info) return STRATA_EINVAL;
   const strata_moe_desc& d = h->desc;
   info->n_sm = h->nsm;
-  info->stages_gateup = h->c_gateup.nstages;
-  info->stages_down = h->c_down.nstages;
-  info->smem_gateup = h->c_gateup.total_bytes;
-  info->smem_down = h->c_down.total_bytes;
+  info->stages = h->cfg.nstages;
+  info->stage_bytes = h->cfg.stage_bytes;
+  info->smem_bytes = h->cfg.total_bytes;
   info->packed_bytes = h->packed;
   info->expert_bytes = qmat_bytes(2, d.ffn, d.hidden, d.bits, d.block) + qmat_bytes(1, d.hidden, d.ffn, d.bits, d.block);
   info->shared_bytes = d.shared_ffn > 0 ? qmat_bytes(2, d.shared_ffn, d.hidden, d.bits, d.block) +
@@ -328,17 +324,12 @@ strata_status strata_window_set_profiling(strata_window* h, int32_t enable) {
   return STRATA_OK;
 }
 
-strata_status strata_window_timings(strata_window* h, float ms[3]) {
+strata_status strata_window_timings(strata_window* h, float* ms) {
   if (!h || !ms || !h->profiled_once) return STRATA_EINVAL;
-  if (cudaEventSynchronize(h->prof[3]) != cudaSuccess) {
+  if (cudaEventSynchronize(h->prof[1]) != cudaSuccess ||
+      cudaEventElapsedTime(ms, h->prof[0], h->prof[1]) != cudaSuccess) {
     cudaGetLastError();
     return STRATA_ECUDA;
-  }
-  for (int i = 0; i < 3; ++i) {
-    if (cudaEventElapsedTime(&ms[i], h->prof[i], h->prof[i + 1]) != cudaSuccess) {
-      cudaGetLastError();
-      return STRATA_ECUDA;
-    }
   }
   return STRATA_OK;
 }

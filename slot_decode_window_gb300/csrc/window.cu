@@ -1,0 +1,1167 @@
+// The verify-window MoE step as one persistent kernel.
+//
+// The Strata docs ("BATCHING.md", "Several requests at once (batch slots)",
+// opening paragraph) state the scheme: a verify window carries one token of
+// each open conversation, and the shared expert and every routed expert that
+// rows of a window share are read once per window for all of them.  Here every
+// distinct expert's packed tiles are streamed from HBM once and multiplied
+// against all of that expert's rows (up to 8) in one pass.  The pages give no
+// formulas; the kernel computes the plain reading stated in strata_window.h.
+//
+// One launch per window, one CTA per SM (cooperative launch, so all CTAs are
+// resident and the few cross-CTA waits below always end):
+//   R. router: every warp takes (expert, 256-column chunk) pairs of the fp32
+//      router GEMV and writes partial logits; all threads turn x into the
+//      activation fragments of the gate/up MMAs.  One grid barrier follows.
+//   P. every CTA sums the partial logits in a fixed order and derives the same
+//      routing plan: fp32 softmax, top-k by logit (ties to the lower expert),
+//      gate weights, counting-sort row groups (bit-exact in every CTA).
+//   0. gate/up: for the shared expert and each distinct routed expert e, for
+//      each 16-row tile of Wg_e, Wu_e: gu = Wg_e x_t, uu = Wu_e x_t for every
+//      row t of e's group, written in fp32.  Each finished task bumps its
+//      group's completion counter.
+//   1. down: a CTA starts a group's down tiles once that group's gate/up tasks
+//      have all landed (bounded wait on the counter; the weights stream in
+//      meanwhile); h = silu(gu) * uu is formed while staging the group; then
+//      o = g_tj * (Wd_e h), or s_t = Wsd h_t for the shared expert.  The CTA
+//      whose contribution to a 16-row slice of y lands last sums
+//      y_t = s_t + sum_j o_tj in a fixed order.
+//
+// Within a CTA a producer warp streams k-chunks of each task's tiles into a
+// shared-memory ring with bulk async copies; 16 consumer warps split the
+// task's sub-tiles and k-steps.  A consumer turns packed codes into fp16
+// subnormals (one AND per code pair), multiplies them against the rows'
+// activations with mma.sync m16n8k16 (activations split into fp16 hi + lo
+// parts so the products keep fp32-level accuracy), applies each block's scale
+// to the fp32 accumulator fragment, and adds the min term with one more MMA
+// against per-block activation sums.  Lanes whose activation columns are
+// unused (groups of fewer than 4 or 8 rows) skip their operand loads.
+#include "common.cuh"
+#include "frag.cuh"
+#include "kernels.h"
+
+namespace strata {
+
+namespace {
+
+constexpr int kMaxSub = 4;  // sub-tiles per task
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr long long kWaitCycles = 1LL << 31;  // about a second at GB300 clocks
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigned* err, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (*abort_flag) return false;
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(err, kErrTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Shared-memory activation (B operand) layout, per set (hi, or lo when rows > 4):
+//   main: k-step ks holds S/8 planes of 256 halves; in plane p, column col
+//         (0..7) and lane quad c (0..3) own 8 halves at (col*4 + c)*8, so a
+//         warp's 16-byte loads of one plane are contiguous (no bank conflicts).
+//   sums: min group mk holds 16 halves per column: (mk*8 + col)*16 + c*4.
+template <int BITS>
+__device__ __forceinline__ int bmain_off(int ks, int p, int col, int c) {
+  return ks * 32 * Fmt<BITS>::kBHalves + p * 256 + (col * 4 + c) * 8;
+}
+
+// One k-step of one sub-tile.  acc is in units of 2^-24 (subnormal codes).
+// bk points at this lane's slot of plane 0 of the k-step (set 0).
+template <int BITS, bool PAIRED>
+__device__ __forceinline__ void kstep_mma(const uint8_t* __restrict__ ch, const __half* __restrict__ bk, int bm_set,
+                                          bool bon, int lane, float (&acc)[4]) {
+  const int g = lane >> 2;
+  const float z4[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  if constexpr (BITS == 4) {
+    const uint4 bA = bon ? *reinterpret_cast<const uint4*>(bk) : z;
+    const uint4 bB = bon ? *reinterpret_cast<const uint4*>(bk + 256) : z;
+    uint4 lA = bA, lB = bB;
+    if constexpr (!PAIRED) {
+      lA = bon ? *reinterpret_cast<const uint4*>(bk + bm_set) : z;
+      lB = bon ? *reinterpret_cast<const uint4*>(bk + bm_set + 256) : z;
+    }
+    const uint4 cw = *reinterpret_cast<const uint4*>(ch + lane * 16);
+    const uint2 sr = *reinterpret_cast<const uint2*>(ch + 512 + g * 8);
+    const float2 sg = __half22float2(*reinterpret_cast<const __half2*>(&sr.x));
+    const float2 s8 = __half22float2(*reinterpret_cast<const __half2*>(&sr.y));
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      const uint32_t wg = blk ? cw.z : cw.x, w8 = blk ? cw.w : cw.y;
+      const uint32_t wg2 = wg >> 8, w82 = w8 >> 8;
+      const uint4 b = blk ? bB : bA;
+      float d[4];
+      mma16816(d, dq_pair(wg, 0x000F000Fu), dq_pair(w8, 0x000F000Fu), dq_pair(wg2, 0x000F000Fu),
+               dq_pair(w82, 0x000F000Fu), b.x, b.y, z4);
+      mma16816(d, dq_pair(wg, 0x00F000F0u), dq_pair(w8, 0x00F000F0u), dq_pair(wg2, 0x00F000F0u),
+               dq_pair(w82, 0x00F000F0u), b.z, b.w, d);
+      if constexpr (!PAIRED) {
+        const uint4 l = blk ? lB : lA;
+        mma16816(d, dq_pair(wg, 0x000F000Fu), dq_pair(w8, 0x000F000Fu), dq_pair(wg2, 0x000F000Fu),
+                 dq_pair(w82, 0x000F000Fu), l.x, l.y, d);
+        mma16816(d, dq_pair(wg, 0x00F000F0u), dq_pair(w8, 0x00F000F0u), dq_pair(wg2, 0x00F000F0u),
+                 dq_pair(w82, 0x00F000F0u), l.z, l.w, d);
+      }
+      const float sgv = blk ? sg.y : sg.x, s8v = blk ? s8.y : s8.x;
+      acc[0] = fmaf(sgv, d[0], acc[0]);
+      acc[1] = fmaf(sgv, d[1], acc[1]);
+      acc[2] = fmaf(s8v, d[2], acc[2]);
+      acc[3] = fmaf(s8v, d[3], acc[3]);
+    }
+  } else {
+    const uint4 cw = *reinterpret_cast<const uint4*>(ch + lane * 16);
+    const uint4 sa = *reinterpret_cast<const uint4*>(ch + 512 + g * 32);       // s(g, b0..b7)
+    const uint4 sb = *reinterpret_cast<const uint4*>(ch + 512 + g * 32 + 16);  // s(g+8, b0..b7)
+    const uint32_t cwv[4] = {cw.x, cw.y, cw.z, cw.w};
+    const uint32_t sav[4] = {sa.x, sa.y, sa.z, sa.w};
+    const uint32_t sbv[4] = {sb.x, sb.y, sb.z, sb.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 b = bon ? *reinterpret_cast<const uint4*>(bk + 256 * j) : z;
+      uint4 l = b;
+      if constexpr (!PAIRED) l = bon ? *reinterpret_cast<const uint4*>(bk + bm_set + 256 * j) : z;
+      const uint32_t w = cwv[j], w2 = w >> 8;
+      const float2 sgp = __half22float2(*reinterpret_cast<const __half2*>(&sav[j]));
+      const float2 s8p = __half22float2(*reinterpret_cast<const __half2*>(&sbv[j]));
+      float d[4];
+      mma16816(d, dq_pair(w, 0x00030003u), dq_pair(w2, 0x00030003u), dq_pair(w, 0x000C000Cu),
+               dq_pair(w2, 0x000C000Cu), b.x, b.y, z4);
+      if constexpr (!PAIRED)
+        mma16816(d, dq_pair(w, 0x00030003u), dq_pair(w2, 0x00030003u), dq_pair(w, 0x000C000Cu),
+                 dq_pair(w2, 0x000C000Cu), l.x, l.y, d);
+      acc[0] = fmaf(sgp.x, d[0], acc[0]);
+      acc[1] = fmaf(sgp.x, d[1], acc[1]);
+      acc[2] = fmaf(s8p.x, d[2], acc[2]);
+      acc[3] = fmaf(s8p.x, d[3], acc[3]);
+      mma16816(d, dq_pair(w, 0x00300030u), dq_pair(w2, 0x00300030u), dq_pair(w, 0x00C000C0u),
+               dq_pair(w2, 0x00C000C0u), b.z, b.w, z4);
+      if constexpr (!PAIRED)
+        mma16816(d, dq_pair(w, 0x00300030u), dq_pair(w2, 0x00300030u), dq_pair(w, 0x00C000C0u),
+                 dq_pair(w2, 0x00C000C0u), l.z, l.w, d);
+      acc[0] = fmaf(sgp.y, d[0], acc[0]);
+      acc[1] = fmaf(sgp.y, d[1], acc[1]);
+      acc[2] = fmaf(s8p.y, d[2], acc[2]);
+      acc[3] = fmaf(s8p.y, d[3], acc[3]);
+    }
+  }
+}
+
+// This warp's share of one staged chunk of its sub-tile: k-steps [k0, k1)
+// (chunk-local, tile k-step ks_base + kl) and min groups [m0, m1) (chunk-local,
+// tile group mk_base + ml).
+template <int BITS, bool PAIRED>
+__device__ __forceinline__ void chunk_mma(const uint8_t* __restrict__ sub, int mins_off, int ks_base, int k0, int k1,
+                                          int mk_base, int m0, int m1, const __half* __restrict__ bm,
+                                          const __half* __restrict__ bs, int bm_set, int bs_set, bool bon, int lane,
+                                          float (&acc)[4], float (&accm)[4]) {
+  constexpr int S = Fmt<BITS>::kBHalves;
+  const uint8_t* a = sub + k0 * Fmt<BITS>::kChunk;
+  const __half* bk = bm + (ks_base + k0) * 32 * S + lane * 8;
+#pragma unroll 2
+  for (int kl = k0; kl < k1; ++kl) {
+    kstep_mma<BITS, PAIRED>(a, bk, bm_set, bon, lane, acc);
+    a += Fmt<BITS>::kChunk;
+    bk += 32 * S;
+  }
+  const uint8_t* am_p = sub + mins_off + m0 * 512 + lane * 16;
+  const __half* sp = bs + (mk_base + m0) * 128 + lane * 4;
+  const uint2 z = make_uint2(0u, 0u);
+  for (int ml = m0; ml < m1; ++ml) {
+    const uint2 b = bon ? *reinterpret_cast<const uint2*>(sp) : z;
+    const uint4 am = *reinterpret_cast<const uint4*>(am_p);
+    mma16816(accm, am.x, am.y, am.z, am.w, b.x, b.y, accm);
+    if constexpr (!PAIRED) {
+      const uint2 l = bon ? *reinterpret_cast<const uint2*>(sp + bs_set) : z;
+      mma16816(accm, am.x, am.y, am.z, am.w, l.x, l.y, accm);
+    }
+    am_p += 512;
+    sp += 128;
+  }
+}
+
+// Task layout of one phase.
+struct PhaseTasks {
+  int ntask_s;  // tasks of the shared expert
+  int ntask_e;  // tasks of each routed expert
+  int mt;       // 16-row tiles per task
+  int t0, t1;   // this CTA's task range
+};
+
+// Routing plan and task map, cached in shared memory for the whole kernel.
+struct SPlan {
+  int nd;
+  int distinct[kMaxExperts];
+  int counts[kMaxExperts];
+  int offsets[kMaxExperts];
+  int entries[kMaxEntries];
+  int sel[kMaxEntries];
+  float topk_w[kMaxEntries];
+  int wscan[32];
+  int wcnt[2][kMaxExperts];         // per-warp expert counts of the grouping pass
+  int finish[kMaxEntries * 4];      // row slices this CTA combines
+  int nfinish;
+  int ok;                           // the grid barrier passed
+  PhaseTasks pt[2];
+};
+
+__device__ __forceinline__ unsigned ord_f32(float f) {
+  const unsigned u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unord_f32(unsigned u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
+// ---------------------------------------------------------------------------
+// stage R: router partial logits and x fragments (all threads of all CTAs)
+// ---------------------------------------------------------------------------
+template <int BITS>
+__device__ void write_x_frags(const LayerDev& L, const WindowBufs& W) {
+  constexpr int B = Fmt<BITS>::kBlock;
+  const int d = L.d;
+  const int nmk = (d / B + 15) / 16;
+  const long long fh = frag_halves(d, nmk);
+  const long long n_el = (long long)W.T * d;  // a multiple of 64: warps never straddle a block or a row
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long n_iter = (n_el + stride - 1) / stride;
+  for (long long it = 0; it < n_iter; ++it) {
+    const long long i = tid + it * stride;
+    const bool in = i < n_el;
+    const int t = in ? (int)(i / d) : 0, j = in ? (int)(i % d) : 0;
+    const float v = in ? W.x[i] : 0.f;
+    __half* base = W.xfrag + t * fh;
+    if (in) {
+      int off;
+      float f;
+      frag_main_pos<BITS>(j, off, f);
+      __half hi, lo;
+      split_hi_lo(v * f, hi, lo);
+      base[off] = hi;
+      base[d + off] = lo;
+    }
+    float s = v;
+#pragma unroll
+    for (int o = B / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (in && (j % B) == 0) {
+      __half hi, lo;
+      split_hi_lo(s, hi, lo);
+      const int off = frag_sum_pos(j / B);
+      base[2 * d + off] = hi;
+      base[2 * d + nmk * 16 + off] = lo;
+    }
+  }
+}
+
+template <int BITS>
+__device__ __noinline__ void router_stage(const LayerDev& L, const WindowBufs& W) {
+  const int T = W.T, d = L.d, E = L.E;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  const int npairs = E * W.njb;
+  for (int p = warp * gridDim.x + blockIdx.x; p < npairs; p += gridDim.x * nwarps) {
+    const int e = p % E, jb = p / E;  // pairs spread over all CTAs
+    const int j0 = jb * kRouterCols, ncol = min(kRouterCols, d - j0);
+    float acc[kMaxRows];
+#pragma unroll
+    for (int t = 0; t < kMaxRows; ++t) acc[t] = 0.f;
+    const float* wr = L.router_w + (long long)e * d + j0;
+    for (int j = lane * 4; j < ncol; j += 128) {
+      const float4 w4 = *reinterpret_cast<const float4*>(wr + j);
+#pragma unroll
+      for (int t = 0; t < kMaxRows; ++t) {
+        if (t < T) {
+          const float4 x4 = __ldg(reinterpret_cast<const float4*>(W.x + (long long)t * d + j0 + j));
+          acc[t] = fmaf(w4.x, x4.x, acc[t]);
+          acc[t] = fmaf(w4.y, x4.y, acc[t]);
+          acc[t] = fmaf(w4.z, x4.z, acc[t]);
+          acc[t] = fmaf(w4.w, x4.w, acc[t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kMaxRows; ++t) {
+      float v = acc[t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == t && t < T) W.partial[((long long)jb * kMaxRows + t) * E + e] = v;
+    }
+  }
+  write_x_frags<BITS>(L, W);
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < d / 16; i += blockDim.x) W.counters[i] = 0;
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) W.done_gu[i] = 0;
+  }
+}
+
+// All CTAs arrive; thread 0 waits (bounded) until every CTA of this window has.
+// The counter only grows: the window's target is the next multiple of the grid.
+__device__ bool grid_barrier(const WindowBufs& W, int* s_ok) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned long long n = gridDim.x;
+    const unsigned long long old = atomicAdd(W.gbar, 1ull);
+    const unsigned long long target = (old / n + 1) * n;
+    const long long t0 = clock64();
+    int ok = 1;
+    while (ld_acquire_u64(W.gbar) < target) {
+      if (clock64() - t0 > kWaitCycles) {
+        atomicOr(W.err, kErrTimeout);
+        ok = 0;
+        break;
+      }
+      __nanosleep(64);
+    }
+    __threadfence();
+    *s_ok = ok;
+  }
+  __syncthreads();
+  return *s_ok != 0;
+}
+
+// ---------------------------------------------------------------------------
+// stage P: the routing plan (every CTA, same fixed-order arithmetic)
+// ---------------------------------------------------------------------------
+__device__ __noinline__ void compute_plan(const LayerDev& L, const WindowBufs& W, SPlan& sp, float* lg) {
+  const int T = W.T, E = L.E, k = L.k, njb = W.njb;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool pub = blockIdx.x == 0;
+  // 1. logits: the column-chunk partials summed in chunk order, loads batched
+  for (int i = tid; i < T * E; i += blockDim.x) {
+    const int t = i / E, e = i - t * E;
+    const float* pp = W.partial + (long long)t * E + e;
+    float v = 0.f;
+    for (int b0 = 0; b0 < njb; b0 += 16) {
+      float part[16];
+#pragma unroll
+      for (int b = 0; b < 16; ++b)
+        part[b] = (b0 + b < njb) ? __ldcg(pp + (long long)(b0 + b) * kMaxRows * E) : 0.f;
+#pragma unroll
+      for (int b = 0; b < 16; ++b) v += part[b];
+    }
+    if (L.router_b) v += L.router_b[e];
+    lg[t * E + e] = v;
+  }
+  __syncthreads();
+  // 2. top-k by logit (descending, ties -> lower expert index) and the fp32
+  //    softmax weights of the chosen experts; warp t owns row t, its logits in
+  //    registers (E <= 256: eight per lane)
+  if (warp < T) {
+    const float* lr = lg + warp * E;
+    unsigned key[kMaxExperts / 32];
+    float val[kMaxExperts / 32];
+    bool finite = true;
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = lane + 32 * i;
+      val[i] = e < E ? lr[e] : 0.f;
+      finite &= isfinite(val[i]);
+      key[i] = e < E ? ord_f32(val[i]) : 0u;  // 0: below every real logit
+    }
+    if (!__all_sync(0xffffffffu, finite) && lane == 0 && pub) atomicOr(W.err, kErrNonFinite);
+    int esel = 0;
+    float lsel = 0.f, top = 0.f;
+    for (int j = 0; j < k; ++j) {
+      unsigned bk = 0u;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i)
+        if (key[i] > bk) { bk = key[i]; be = lane + 32 * i; }
+      const unsigned kmax = __reduce_max_sync(0xffffffffu, bk);
+      int bi = (int)__reduce_min_sync(0xffffffffu, (bk == kmax && be != 0x7fffffff) ? (unsigned)be : 0xffffffffu);
+      if (bi < 0 || bi >= E) bi = 0;  // only with non-finite logits
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i)
+        if (lane + 32 * i == bi) key[i] = 0u;
+      const float lv = unord_f32(kmax);
+      if (j == 0) top = lv;
+      if (lane == j) { esel = bi; lsel = lv; }
+    }
+    // softmax over all E logits, shifted by the largest
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i)
+      if (lane + 32 * i < E) z += expf(val[i] - top);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    const float p = lane < k ? expf(lsel - top) / z : 0.f;
+    float wsum = p;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    if (lane < k) {
+      const float g = L.renorm ? p / wsum : p;
+      const int ent = warp * k + lane;
+      sp.sel[ent] = esel;
+      sp.topk_w[ent] = g;
+      if (pub) {
+        if (W.out_topk_idx) W.out_topk_idx[ent] = esel;
+        if (W.out_topk_w) W.out_topk_w[ent] = g;
+      }
+    }
+  }
+  __syncthreads();
+  // 3. grouping: entries ordered by expert, then by entry index.  Warps 0 and 1
+  //    hold entries 0..31 and 32..63; match_any gives each entry its rank among
+  //    the same expert's entries of its warp and each warp's per-expert count.
+  const int nent = T * k;
+  const int n_me = warp * 32 + lane;
+  const bool has_ent = warp < 2 && n_me < nent;
+  const int e_me = has_ent ? sp.sel[n_me] : -1 - lane;  // distinct dummies never match
+  int rank_me = 0;
+  if (warp < 2) {
+    const unsigned peers = __match_any_sync(0xffffffffu, e_me);
+    rank_me = __popc(peers & ((1u << lane) - 1u));
+    if (has_ent && rank_me == 0) sp.wcnt[warp][e_me] = __popc(peers);
+  }
+  __syncthreads();
+  // counts (low 16 bits) and "used" flags (high 16 bits) scanned together
+  const int e = tid;
+  const int c = e < E ? sp.wcnt[0][e] + sp.wcnt[1][e] : 0;
+  const int flag = c > 0 ? 1 : 0;
+  int v = c | (flag << 16);
+  if (tid < kMaxExperts) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += n;
+    }
+    if (lane == 31) sp.wscan[warp] = v;
+  }
+  __syncthreads();
+  if (e < E) {
+    int before = 0;
+#pragma unroll
+    for (int w = 0; w < kMaxExperts / 32; ++w) before += w < warp ? sp.wscan[w] : 0;
+    const int incl = v + before;
+    const int off = (incl & 0xffff) - c, rank = (incl >> 16) - flag;
+    sp.counts[e] = c;
+    sp.offsets[e] = off;
+    if (flag) sp.distinct[rank] = e;
+    if (e == E - 1) sp.nd = incl >> 16;
+    if (pub) {
+      if (W.out_counts) W.out_counts[e] = c;
+      if (W.out_offsets) W.out_offsets[e] = off;
+      if (flag && W.out_distinct) W.out_distinct[rank] = e;
+      if (e == E - 1) {
+        if (W.out_offsets) W.out_offsets[E] = off + c;
+        if (W.out_ndistinct) *W.out_ndistinct = incl >> 16;
+      }
+    }
+  }
+  __syncthreads();
+  if (has_ent) {
+    const int pos = sp.offsets[e_me] + (warp == 1 ? sp.wcnt[0][e_me] : 0) + rank_me;
+    sp.entries[pos] = n_me;
+    if (pub && W.out_entries) W.out_entries[pos] = n_me;
+  }
+}
+
+struct Task {
+  bool shared;
+  int expert;
+  int group;  // shared expert first (when present), then distinct experts ascending
+  int tile;   // first row tile
+};
+
+__device__ __forceinline__ Task decode_task(int task, const PhaseTasks& pt, bool has_shared, const SPlan& sp) {
+  Task t;
+  if (task < pt.ntask_s) {
+    t.shared = true;
+    t.expert = -1;
+    t.group = 0;
+    t.tile = task * pt.mt;
+  } else {
+    const int q = task - pt.ntask_s;
+    const int gi = q / pt.ntask_e;
+    t.shared = false;
+    t.expert = sp.distinct[gi];
+    t.group = gi + (has_shared ? 1 : 0);
+    t.tile = (q - gi * pt.ntask_e) * pt.mt;
+  }
+  return t;
+}
+
+// Estimated cost of one task of a group of R rows (groups of more than 4 rows
+// take the two-set path: twice the MMAs and activation loads).
+__device__ __forceinline__ int task_cost(int R) { return R <= 4 ? 2 : 3; }
+
+// Contiguous task ranges of equal estimated cost (one warp): each lane takes a
+// run of consecutive groups, a warp scan gives every group its starting cost
+// position, and the lane whose groups hold a range boundary reports the task.
+__device__ __forceinline__ void split_tasks(const WindowBufs& W, SPlan& sp, bool has_shared, PhaseTasks& pt, int lane) {
+  const int hs = has_shared ? 1 : 0;
+  const int ng = hs + sp.nd;
+  const int ntotal = hs * pt.ntask_s + sp.nd * pt.ntask_e;
+  const int per = (ng + 31) >> 5;
+  const int g0 = lane * per;
+  auto cost_of = [&](int g, int& nt, int& cst) {
+    const bool sh = has_shared && g == 0;
+    nt = sh ? pt.ntask_s : pt.ntask_e;
+    cst = task_cost(sh ? W.T : sp.counts[sp.distinct[g - hs]]);
+  };
+  int run = 0;
+  for (int i = 0; i < per; ++i) {
+    const int g = g0 + i;
+    if (g < ng) {
+      int nt, cst;
+      cost_of(g, nt, cst);
+      run += nt * cst;
+    }
+  }
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  int res[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int P = (int)((long long)total * (blockIdx.x + q) / gridDim.x);
+    int found = -1, pos = incl - run;
+    for (int i = 0; i < per; ++i) {
+      const int g = g0 + i;
+      if (g < ng) {
+        int nt, cst;
+        cost_of(g, nt, cst);
+        const int len = nt * cst;
+        if (P >= pos && P < pos + len) {
+          const int first = (g < hs) ? 0 : hs * pt.ntask_s + (g - hs) * pt.ntask_e;
+          const int j = (P - pos + cst - 1) / cst;
+          found = first + (j < nt ? j : nt);
+        }
+        pos += len;
+      }
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, found >= 0);
+    res[q] = bal ? __shfl_sync(0xffffffffu, found, __ffs(bal) - 1) : ntotal;
+  }
+  if (lane == 0) {
+    pt.t0 = res[0];
+    pt.t1 = res[1];
+  }
+  __syncwarp();
+}
+
+// Stage one group's activations into shared memory (all consumer threads).
+// Phase 0: copy the x fragments.  Phase 1: form h = silu(gu) * uu, its fp16
+// hi/lo fragments and its block sums.
+template <int BITS, int PHASE>
+__device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan& sp, const KernelCfg& C, __half* bm,
+                             __half* bs, bool is_shared, int R, int ent_off, int K, int ctid) {
+  constexpr int S = Fmt<BITS>::kBHalves;
+  constexpr int B = Fmt<BITS>::kBlock;
+  const int nks = K / Fmt<BITS>::kKstep;
+  const int nmk = (K / B + 15) / 16;
+  const bool paired = R <= 4;
+  if (PHASE == 0) {
+    const long long fh = frag_halves(K, nmk);
+    const int nsets = paired ? 1 : 2;
+    const int ncols = paired ? 2 * R : R;
+    // main: 16-byte pieces (ks, c, plane) of each used column
+    const int per_col = nks * 4 * (S / 8);
+    for (int i = ctid; i < nsets * ncols * per_col; i += kConsumerThreads) {
+      const int cs = i / per_col, rem = i - cs * per_col;
+      const int set = cs / ncols, col = cs - set * ncols;
+      const int r = paired ? (col >> 1) : col;
+      const int part = paired ? (col & 1) : set;
+      const int xrow = is_shared ? r : sp.entries[ent_off + r] / L.k;
+      const int ks = rem / (4 * (S / 8)), cp = rem - ks * 4 * (S / 8);
+      const int c = cp / (S / 8), p = cp - c * (S / 8);
+      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(W.xfrag + xrow * fh + (long long)part * K + ks * 4 * S +
+                                                            c * S + p * 8));
+      *reinterpret_cast<uint4*>(bm + set * C.bmain_halves + bmain_off<BITS>(ks, p, col, c)) = v;
+    }
+    // sums: 8-byte pieces (mk, c)
+    for (int i = ctid; i < nsets * ncols * nmk * 4; i += kConsumerThreads) {
+      const int cs = i / (nmk * 4), rem = i - cs * nmk * 4;
+      const int set = cs / ncols, col = cs - set * ncols;
+      const int r = paired ? (col >> 1) : col;
+      const int part = paired ? (col & 1) : set;
+      const int xrow = is_shared ? r : sp.entries[ent_off + r] / L.k;
+      const int mk = rem >> 2, c = rem & 3;
+      const uint2 v = __ldcg(reinterpret_cast<const uint2*>(W.xfrag + xrow * fh + 2LL * K +
+                                                            (long long)part * 16 * nmk + mk * 16 + c * 4));
+      *reinterpret_cast<uint2*>(bs + set * C.bsum_halves + (mk * 8 + col) * 16 + c * 4) = v;
+    }
+  } else {
+    // one element per thread and step; a warp covers 32 consecutive elements of
+    // one row (K is a multiple of 64), so block sums come from lane shuffles
+    for (int i0 = 0; i0 < R * K; i0 += kConsumerThreads) {
+      const int i = i0 + ctid;
+      const bool in = i < R * K;
+      const int r = in ? i / K : 0, f = in ? i - r * K : 0;
+      float h = 0.f;
+      if (in) {
+        const float2* src = is_shared ? W.sgu + (long long)r * L.Fs : W.gu + (long long)sp.entries[ent_off + r] * L.F;
+        const float2 gu = __ldcg(src + f);
+        h = silu_f32(gu.x) * gu.y;
+        int off;
+        float fac;
+        frag_main_pos<BITS>(f, off, fac);
+        const int ks = off / (4 * S), c = (off / S) & 3, slot = off % S;
+        __half hi, lo;
+        split_hi_lo(h * fac, hi, lo);
+        const int o = bmain_off<BITS>(ks, slot >> 3, 0, c) + (slot & 7);
+        if (paired) {
+          bm[o + (2 * r) * 32] = hi;
+          bm[o + (2 * r + 1) * 32] = lo;
+        } else {
+          bm[o + r * 32] = hi;
+          bm[C.bmain_halves + o + r * 32] = lo;
+        }
+      }
+      float s = h;
+#pragma unroll
+      for (int o = B / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (in && (f % B) == 0) {
+        const int spos = frag_sum_pos(f / B);
+        const int mk = spos >> 4, c = (spos >> 2) & 3, slot = spos & 3;
+        __half hi, lo;
+        split_hi_lo(s, hi, lo);
+        const int o = mk * 128 + c * 4 + slot;
+        if (paired) {
+          bs[o + (2 * r) * 16] = hi;
+          bs[o + (2 * r + 1) * 16] = lo;
+        } else {
+          bs[o + r * 16] = hi;
+          bs[C.bsum_halves + o + r * 16] = lo;
+        }
+      }
+    }
+  }
+}
+
+// Ring state shared by the producer and the consumers.
+struct Ring {
+  uint8_t* base;
+  uint64_t* full;
+  uint64_t* empty;
+  volatile int* abort_flag;
+};
+
+// Position in the stage ring: slot, parity of the current lap, slots passed.
+struct RingPos {
+  int stage = 0;
+  uint32_t parity = 0;
+  int n = 0;
+  __device__ __forceinline__ void advance(int nstages) {
+    ++n;
+    if (++stage == nstages) {
+      stage = 0;
+      parity ^= 1u;
+    }
+  }
+};
+
+// Walks a CTA's contiguous task range without dividing: decode the first
+// task once, then step through the groups' task lists.
+struct TaskWalk {
+  Task tk;
+  int j;  // task index inside its group
+  __device__ __forceinline__ void start(int task, const PhaseTasks& pt, bool has_shared, const SPlan& sp) {
+    tk = decode_task(task, pt, has_shared, sp);
+    j = tk.tile / pt.mt;
+  }
+  __device__ __forceinline__ void next(const PhaseTasks& pt, bool has_shared, const SPlan& sp) {
+    ++j;
+    if (tk.shared) {
+      if (j == pt.ntask_s) {
+        j = 0;
+        tk.shared = false;
+        tk.group = 1;
+        tk.expert = sp.distinct[0];
+      }
+    } else if (j == pt.ntask_e) {
+      j = 0;
+      ++tk.group;
+      const int gi = tk.group - (has_shared ? 1 : 0);
+      tk.expert = gi < sp.nd ? sp.distinct[gi] : -1;
+    }
+    tk.tile = j * pt.mt;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// producer: one thread streams every task's k-chunks, phase 0 then phase 1
+// ---------------------------------------------------------------------------
+template <int BITS, int PHASE, int NS>
+__device__ bool produce(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, const SPlan& sp, const Ring& rg,
+                        RingPos& rp) {
+  constexpr int kMT = PHASE == 0 ? NS / 2 : NS;
+  const PhaseCfg& P = C.ph[PHASE];
+  const PhaseTasks& pt = sp.pt[PHASE];
+  const bool has_shared = L.Fs > 0;
+  TaskWalk tw;
+  if (pt.t0 < pt.t1) tw.start(pt.t0, pt, has_shared, sp);
+  for (int task = pt.t0; task < pt.t1; ++task, tw.next(pt, has_shared, sp)) {
+    const Task& tk = tw.tk;
+    if (!tk.shared && (unsigned)tk.expert >= (unsigned)L.E) {
+      atomicOr(W.err, kErrIndex);
+      *rg.abort_flag = 1;
+      return false;
+    }
+    const int K = PHASE == 0 ? L.d : (tk.shared ? L.Fs : L.F);
+    const int nks = K / Fmt<BITS>::kKstep, nmk = (K / Fmt<BITS>::kBlock + 15) / 16;
+    const int tbytes = nks * Fmt<BITS>::kChunk + nmk * 512;
+    const int kv = (PHASE == 1 && tk.shared) ? 1 : 0;
+    for (int ch = 0; ch < P.nchunks; ++ch) {
+      const int ks0 = P.cks[kv][ch], ks1 = P.cks[kv][ch + 1];
+      const int mk0 = P.cmk[kv][ch], mk1 = P.cmk[kv][ch + 1];
+      const int stage = rp.stage;
+      if (rp.n >= C.nstages && !wait_bar(&rg.empty[stage], rp.parity ^ 1u, W.err, rg.abort_flag)) return false;
+      const uint32_t cbytes = (uint32_t)((ks1 - ks0) * Fmt<BITS>::kChunk), mbytes = (uint32_t)((mk1 - mk0) * 512);
+      mbar_arrive_expect_tx(&rg.full[stage], NS * (cbytes + mbytes));
+      uint8_t* dst = rg.base + (size_t)stage * C.stage_bytes;
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        const bool up = PHASE == 0 && s >= kMT;
+        const PackedMat& M = PHASE == 0 ? (up ? (tk.shared ? L.sup : L.up) : (tk.shared ? L.sgate : L.gate))
+                                        : (tk.shared ? L.sdown : L.down);
+        const int tile = tk.tile + (up ? s - kMT : s);
+        const uint8_t* src =
+            M.base + (tk.shared ? 0LL : (long long)tk.expert * M.mat_bytes) + (long long)tile * tbytes;
+        uint8_t* dd = dst + s * P.sub_stride;
+        if (cbytes) bulk_g2s(dd, src + (size_t)ks0 * Fmt<BITS>::kChunk, cbytes, &rg.full[stage]);
+        if (mbytes) bulk_g2s(dd + P.mins_off, src + (size_t)nks * Fmt<BITS>::kChunk + mk0 * 512, mbytes, &rg.full[stage]);
+      }
+      rp.advance(C.nstages);
+    }
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// consumers: one phase's tasks (all 16 consumer warps)
+// ---------------------------------------------------------------------------
+// One output of an accumulator fragment: element idx (paired: the hi + lo
+// columns idx and idx + 1).  Selects, not an indexed array, so the fragment
+// stays in registers.
+__device__ __forceinline__ float frag_pick(const float4 a, int idx, bool paired) {
+  const float lo = (idx & 2) ? a.z : a.x, hi = (idx & 2) ? a.w : a.y;
+  return paired ? lo + hi : ((idx & 1) ? hi : lo);
+}
+
+template <int BITS, int PHASE, int NS>
+__device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, SPlan& sp, const Ring& rg,
+                        __half* bm, __half* bs, float4* red, RingPos& rp, int& buf) {
+  constexpr int kMT = PHASE == 0 ? NS / 2 : NS;  // row tiles per task
+  constexpr int kWPS = kConsumerWarps / NS;      // warps per sub-tile
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const PhaseCfg& P = C.ph[PHASE];
+  const PhaseTasks& pt = sp.pt[PHASE];
+  const bool has_shared = L.Fs > 0;
+  const int sub = warp / kWPS, kg = warp % kWPS;
+  const int g = lane >> 2;
+  int cur = -2;
+  int R = 0, ent_off = 0;
+  bool paired = true, bon = true;
+  uint32_t inv_d = 0;  // ceil(2^16 / (16 R)): i / (16 R) == (i * inv_d) >> 16 for i < 512
+  TaskWalk tw;
+  if (pt.t0 < pt.t1) tw.start(pt.t0, pt, has_shared, sp);
+  for (int task = pt.t0; task < pt.t1; ++task, tw.next(pt, has_shared, sp)) {
+    const Task& tk = tw.tk;
+    if (!tk.shared && (unsigned)tk.expert >= (unsigned)L.E) break;  // flagged by the producer
+    const int K = PHASE == 0 ? L.d : (tk.shared ? L.Fs : L.F);
+    if (tk.group != cur) {
+      if (tk.shared) {
+        R = W.T;
+        ent_off = 0;
+      } else {
+        R = sp.counts[tk.expert];
+        ent_off = sp.offsets[tk.expert];
+      }
+      if (R < 1 || R > kMaxRows) {
+        atomicOr(W.err, kErrIndex);
+        R = R < 1 ? 1 : kMaxRows;
+      }
+      paired = R <= 4;
+      bon = paired ? (g < 2 * R) : (g < R);
+      inv_d = (65536u + 16u * R - 1u) / (16u * R);
+      if (PHASE == 1) {
+        // wait (bounded) until every gate/up task of this group has landed
+        if (tid == 0) {
+          const int need = tk.shared ? sp.pt[0].ntask_s : sp.pt[0].ntask_e;
+          const long long t0 = clock64();
+          while (!*rg.abort_flag && ld_acquire(W.done_gu + tk.group) < need) {
+            if (clock64() - t0 > kWaitCycles) {
+              atomicOr(W.err, kErrTimeout);
+              *rg.abort_flag = 1;
+              break;
+            }
+            __nanosleep(32);
+          }
+        }
+        consumer_sync();
+      }
+      // the previous task's barrier guarantees no warp still reads the old fragments
+      load_group_B<BITS, PHASE>(L, W, sp, C, bm, bs, tk.shared, R, ent_off, K, tid);
+      consumer_sync();
+      cur = tk.group;
+    }
+    const int kv = (PHASE == 1 && tk.shared) ? 1 : 0;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int ch = 0; ch < P.nchunks; ++ch) {
+      const int ks0 = P.cks[kv][ch], ks1 = P.cks[kv][ch + 1];
+      const int mk0 = P.cmk[kv][ch], mk1 = P.cmk[kv][ch + 1];
+      const int nk = ks1 - ks0, nm = mk1 - mk0;
+      const int k0 = (kg * nk) / kWPS, k1 = ((kg + 1) * nk) / kWPS;
+      const int m0 = (kg * nm) / kWPS, m1 = ((kg + 1) * nm) / kWPS;
+      const int stage = rp.stage;
+      if (wait_bar(&rg.full[stage], rp.parity, W.err, rg.abort_flag)) {
+        const uint8_t* st = rg.base + (size_t)stage * C.stage_bytes + sub * P.sub_stride;
+        if (paired)
+          chunk_mma<BITS, true>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves, C.bsum_halves,
+                                bon, lane, acc, accm);
+        else
+          chunk_mma<BITS, false>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves, C.bsum_halves,
+                                 bon, lane, acc, accm);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rg.empty[stage]);
+      rp.advance(C.nstages);
+    }
+    float4* rb = red + buf * (kConsumerWarps * 32);
+    rb[warp * 32 + lane] = make_float4(fmaf(acc[0], kDqUnscale, accm[0]), fmaf(acc[1], kDqUnscale, accm[1]),
+                                       fmaf(acc[2], kDqUnscale, accm[2]), fmaf(acc[3], kDqUnscale, accm[3]));
+    consumer_sync();
+
+    // ---------------- epilogue: cross-warp sums in a fixed order ----------------
+    const int eo = (tid & 31) * kConsumerWarps + (tid >> 5);  // this thread's first output
+    if (PHASE == 0) {
+      for (int i = eo; i < kMT * 16 * R; i += kConsumerThreads) {
+        const int m = (int)(((uint32_t)i * inv_d) >> 16), rem = i - m * 16 * R;
+        const int r = rem >> 4, row = rem & 15;
+        const int src_lane = (row & 7) * 4 + (paired ? r : (r >> 1));
+        const int idx = ((row >> 3) << 1) + (paired ? 0 : (r & 1));
+        float gv = 0.f, uv = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWPS; ++w) {
+          gv += frag_pick(rb[(m * kWPS + w) * 32 + src_lane], idx, paired);
+          uv += frag_pick(rb[((kMT + m) * kWPS + w) * 32 + src_lane], idx, paired);
+        }
+        const int f = (tk.tile + m) * 16 + row;
+        float2* dst = tk.shared ? W.sgu + (long long)r * L.Fs : W.gu + (long long)sp.entries[ent_off + r] * L.F;
+        dst[f] = make_float2(gv, uv);
+      }
+    } else {
+      for (int i = eo; i < NS * 16 * R; i += kConsumerThreads) {
+        const int s = (int)(((uint32_t)i * inv_d) >> 16), rem = i - s * 16 * R;
+        const int r = rem >> 4, row = rem & 15;
+        const int src_lane = (row & 7) * 4 + (paired ? r : (r >> 1));
+        const int idx = ((row >> 3) << 1) + (paired ? 0 : (r & 1));
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWPS; ++w) v += frag_pick(rb[(s * kWPS + w) * 32 + src_lane], idx, paired);
+        const int drow = (tk.tile + s) * 16 + row;
+        if (tk.shared) {
+          W.sbuf[(long long)r * L.d + drow] = v;
+        } else {
+          const int ent = sp.entries[ent_off + r];
+          W.obuf[(long long)ent * L.d + drow] = sp.topk_w[ent] * v;
+        }
+      }
+    }
+    buf ^= 1;
+  }
+  if (PHASE == 0) {
+    // publish this CTA's finished gate/up tasks: one fence, then per-group counts
+    __threadfence();
+    consumer_sync();
+    for (int task = pt.t0 + tid; task < pt.t1; task += kConsumerThreads) {
+      const Task tk = decode_task(task, pt, has_shared, sp);
+      atomicAdd(W.done_gu + tk.group, 1);
+    }
+  }
+}
+
+// Count this CTA's finished row slices of y; the CTA that completes a slice's
+// count sums it in a fixed order (consumer threads).
+template <int NS>
+__device__ void combine(const LayerDev& L, const WindowBufs& W, SPlan& sp) {
+  const int tid = threadIdx.x;
+  const PhaseTasks& pt = sp.pt[1];
+  const bool has_shared = L.Fs > 0;
+  __threadfence();
+  consumer_sync();
+  if (tid == 0) sp.nfinish = 0;
+  consumer_sync();
+  const int ngroups = (has_shared ? 1 : 0) + sp.nd;
+  const int ntiles = (pt.t1 - pt.t0) * NS;
+  // y over 4 consecutive outputs of row t: shared expert first, then the
+  // k weighted expert outputs in entry order (all loads issued up front)
+  auto sum_quad = [&](int tile, int u) {
+    const int t = u >> 2, rr = tile * 16 + (u & 3) * 4;
+    float4 y = has_shared ? __ldcg(reinterpret_cast<const float4*>(W.sbuf + (long long)t * L.d + rr))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 o[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      o[j] = j < L.k ? __ldcg(reinterpret_cast<const float4*>(W.obuf + (long long)(t * L.k + j) * L.d + rr))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < L.k) {
+        y.x += o[j].x;
+        y.y += o[j].y;
+        y.z += o[j].z;
+        y.w += o[j].w;
+      }
+    }
+    *reinterpret_cast<float4*>(W.y + (long long)t * L.d + rr) = y;
+  };
+  for (int i = tid; i < ntiles; i += kConsumerThreads) {
+    const Task tk = decode_task(pt.t0 + i / NS, pt, has_shared, sp);
+    const int tile = tk.tile + i % NS;
+    if (atomicAdd(W.counters + tile, 1) == ngroups - 1) {
+      const int slot = atomicAdd(&sp.nfinish, 1);
+      if (slot < kMaxEntries * 4) {
+        sp.finish[slot] = tile;
+      } else {  // list full: this thread sums the slice itself
+        __threadfence();
+        for (int u = 0; u < W.T * 4; ++u) sum_quad(tile, u);
+      }
+    }
+  }
+  consumer_sync();
+  __threadfence();
+  const int nf = min(sp.nfinish, kMaxEntries * 4);
+  for (int i = tid; i < nf * W.T * 4; i += kConsumerThreads) sum_quad(sp.finish[i / (W.T * 4)], i % (W.T * 4));
+}
+
+}  // namespace
+
+// Shared memory: [ring: nstages x stage_bytes][B main: nsets][B sums: nsets]
+// [red: 2 x 16 warps x 32 lanes float4][full/empty mbarriers]; static: SPlan.
+template <int BITS>
+__global__ void __launch_bounds__(kExpertThreads, 1) window_kernel(LayerDev L, WindowBufs W, KernelCfg C) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ volatile int s_abort;
+  __shared__ SPlan sp;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint8_t* ring = smem;
+  __half* bm = reinterpret_cast<__half*>(smem + (size_t)C.nstages * C.stage_bytes);
+  __half* bs = bm + (size_t)C.nsets * C.bmain_halves;
+  float4* red = reinterpret_cast<float4*>(bs + (size_t)C.nsets * C.bsum_halves);
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * kConsumerWarps * 32);
+  uint64_t* empty = full + kMaxStages;
+  const Ring rg{ring, full, empty, &s_abort};
+
+  if (tid == 0) {
+    for (int s = 0; s < C.nstages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  // padded block-sum slots are never written: zero the sums region once
+  for (int i = tid; i < C.nsets * C.bsum_halves / 2; i += blockDim.x) reinterpret_cast<uint32_t*>(bs)[i] = 0u;
+  for (int i = tid; i < 2 * kMaxExperts; i += blockDim.x) (&sp.wcnt[0][0])[i] = 0;
+
+  // R: router partial logits, x fragments; then every CTA waits for all
+  router_stage<BITS>(L, W);
+  if (!grid_barrier(W, &sp.ok)) return;  // timed out: the error word says so
+
+  // P: the routing plan (the ring is free until the producer starts: logits scratch)
+  compute_plan(L, W, sp, reinterpret_cast<float*>(ring));
+  const int nd = sp.nd;
+  if (nd < 0 || nd > L.E) {
+    if (tid == 0) atomicOr(W.err, kErrIndex);
+    return;
+  }
+  const bool has_shared = L.Fs > 0;
+  if (warp == 0) {
+    // gate/up: 2 row tiles per task when that still leaves >= 3 tasks per CTA
+    PhaseTasks& p0 = sp.pt[0];
+    const int tiles_e = L.F / 16, tiles_s = has_shared ? L.Fs / 16 : 0;
+    const long long all0 = tiles_s + (long long)nd * tiles_e;
+    p0.mt = (C.ph[0].max_sub >= 4 && tiles_e % 2 == 0 && tiles_s % 2 == 0 && all0 / 2 >= 3LL * gridDim.x) ? 2 : 1;
+    p0.ntask_s = tiles_s / p0.mt;
+    p0.ntask_e = tiles_e / p0.mt;
+    split_tasks(W, sp, has_shared, p0, lane);
+  } else if (warp == 1) {
+    // down: as many row tiles per task as keep >= 3 tasks per CTA (up to 4)
+    PhaseTasks& p1 = sp.pt[1];
+    const int tiles_g = L.d / 16;
+    const long long all1 = (long long)((has_shared ? 1 : 0) + nd) * tiles_g;
+    int mt = C.ph[1].max_sub;
+    while (mt > 1 && (tiles_g % mt != 0 || all1 / mt < 3LL * gridDim.x)) mt >>= 1;
+    p1.mt = mt;
+    p1.ntask_s = has_shared ? tiles_g / mt : 0;
+    p1.ntask_e = tiles_g / mt;
+    split_tasks(W, sp, has_shared, p1, lane);
+  }
+  __syncthreads();
+
+  RingPos rp;
+  if (warp == kConsumerWarps) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      const int ns0 = 2 * sp.pt[0].mt, ns1 = sp.pt[1].mt;
+      const bool ok = ns0 == 4 ? produce<BITS, 0, 4>(L, W, C, sp, rg, rp) : produce<BITS, 0, 2>(L, W, C, sp, rg, rp);
+      if (ok) {
+        if (ns1 == 4) produce<BITS, 1, 4>(L, W, C, sp, rg, rp);
+        else if (ns1 == 2) produce<BITS, 1, 2>(L, W, C, sp, rg, rp);
+        else produce<BITS, 1, 1>(L, W, C, sp, rg, rp);
+      }
+      if (s_abort) {
+        // Let every copy this thread issued land before the CTA can exit.
+        const int it = rp.n;
+        for (int j = (it > C.nstages ? it - C.nstages : 0); j < it; ++j) {
+          const long long tw = clock64();
+          while (!mbar_try_wait(&full[j % C.nstages], (j / C.nstages) & 1)) {
+            if (clock64() - tw > kWaitCycles) break;
+          }
+        }
+      }
+    }
+    return;
+  }
+  const int ns0 = 2 * sp.pt[0].mt, ns1 = sp.pt[1].mt;
+  int buf = 0;
+  if (ns0 == 4) consume<BITS, 0, 4>(L, W, C, sp, rg, bm, bs, red, rp, buf);
+  else consume<BITS, 0, 2>(L, W, C, sp, rg, bm, bs, red, rp, buf);
+  if (ns1 == 4) {
+    consume<BITS, 1, 4>(L, W, C, sp, rg, bm, bs, red, rp, buf);
+    combine<4>(L, W, sp);
+  } else if (ns1 == 2) {
+    consume<BITS, 1, 2>(L, W, C, sp, rg, bm, bs, red, rp, buf);
+    combine<2>(L, W, sp);
+  } else {
+    consume<BITS, 1, 1>(L, W, C, sp, rg, bm, bs, red, rp, buf);
+    combine<1>(L, W, sp);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+// Cut one phase's tiles into ring stages: the task width (sub-tiles 4, 2 or 1;
+// gate/up need >= 2) and the fewest k-chunks per tile that fit the stage
+// budget, scored by k-steps per warp per chunk (each chunk costs one wait and
+// one release per warp).
+static PhaseCfg phase_cfg(int phase, int bits, int Kv0, int Kv1, int stage_budget, int& stage_bytes) {
+  const int kstep = bits == 4 ? 64 : 128, block = bits == 4 ? 32 : 16, chunk = bits == 4 ? 576 : 768;
+  const int Kmax = Kv0 > Kv1 ? Kv0 : Kv1;
+  const int nks = Kmax / kstep, nmk = (Kmax / block + 15) / 16;
+  const int ns_min = phase == 0 ? 2 : 1;
+  PhaseCfg best{};
+  int best_score = -1;
+  stage_bytes = 0;
+  for (int ns = kMaxSub; ns >= ns_min; ns >>= 1) {
+    const int wps = kConsumerWarps / ns;
+    for (int nc = 1; nc <= nks && nc <= kMaxChunks; ++nc) {
+      const int cks = (nks + nc - 1) / nc, cmk = (nmk + nc - 1) / nc;
+      const int sub_stride = cks * chunk + cmk * 512;
+      if (ns * sub_stride > stage_budget) continue;
+      const int per_warp = (nks / nc) / wps;
+      const int score = (per_warp > 8 ? 8 : per_warp) * 1000 + ns * 100;
+      if (score > best_score) {
+        best_score = score;
+        best.nchunks = nc;
+        best.sub_stride = sub_stride;
+        best.mins_off = cks * chunk;
+        best.max_sub = ns;
+        stage_bytes = ns * sub_stride;
+      }
+      break;
+    }
+  }
+  if (best_score < 0) {  // even one k-step per chunk does not fit: smallest possible stage
+    best.nchunks = nks < kMaxChunks ? nks : kMaxChunks;
+    const int cks = (nks + best.nchunks - 1) / best.nchunks, cmk = (nmk + best.nchunks - 1) / best.nchunks;
+    best.sub_stride = cks * chunk + cmk * 512;
+    best.mins_off = cks * chunk;
+    best.max_sub = ns_min;
+    stage_bytes = ns_min * best.sub_stride;
+  }
+  for (int v = 0; v < 2; ++v) {
+    const int K = v == 0 ? Kv0 : Kv1;
+    const int nks_v = K / kstep, nmk_v = (K / block + 15) / 16;
+    for (int ch = 0; ch <= best.nchunks; ++ch) {
+      best.cks[v][ch] = (short)(ch * nks_v / best.nchunks);
+      best.cmk[v][ch] = (short)(ch * nmk_v / best.nchunks);
+    }
+  }
+  return best;
+}
+
+KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit) {
+  KernelCfg C{};
+  const int bits = L.bits;
+  const int block = bits == 4 ? 32 : 16;
+  const int Kmax = L.d > (L.F > L.Fs ? L.F : L.Fs) ? L.d : (L.F > L.Fs ? L.F : L.Fs);
+  const int nmk = (Kmax / block + 15) / 16;
+  C.bmain_halves = 8 * Kmax;
+  C.bsum_halves = nmk * 8 * 4 * 4;
+  C.nsets = max_rows > 4 ? 2 : 1;
+  const int fixed = C.nsets * (C.bmain_halves + C.bsum_halves) * 2 + 2 * kConsumerWarps * 32 * 16 + 2 * kMaxStages * 8;
+  const int ring = smem_limit - fixed;
+  const int budget = ring / 3;  // at least three stages in flight
+  int sb0 = 0, sb1 = 0;
+  C.ph[0] = phase_cfg(0, bits, L.d, L.d, budget, sb0);
+  C.ph[1] = phase_cfg(1, bits, L.F, L.Fs > 0 ? L.Fs : L.F, budget, sb1);
+  C.stage_bytes = sb0 > sb1 ? sb0 : sb1;
+  int st = C.stage_bytes > 0 ? ring / C.stage_bytes : 0;
+  C.nstages = st > kMaxStages ? kMaxStages : st;
+  C.total_bytes = C.nstages * C.stage_bytes + fixed;
+  return C;
+}
+
+static const void* window_fn(int bits) {
+  return bits == 4 ? (const void*)window_kernel<4> : (const void*)window_kernel<2>;
+}
+
+cudaError_t window_set_attrs(int bits, int smem_bytes) {
+  return cudaFuncSetAttribute(window_fn(bits), cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+}
+
+int window_blocks_per_sm(int bits, int smem_bytes) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, window_fn(bits), kExpertThreads, smem_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+cudaError_t launch_window(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, int grid, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kExpertThreads);
+  cfg.dynamicSmemBytes = C.total_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (L.bits == 4) return cudaLaunchKernelEx(&cfg, window_kernel<4>, L, W, C);
+  return cudaLaunchKernelEx(&cfg, window_kernel<2>, L, W, C);
+}
+
+}  // namespace strata

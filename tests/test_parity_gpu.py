@@ -159,6 +159,6 @@ def test_forward_argument_errors_on_device_handle():
     assert B.strata_moe_window_forward(win.handle, x.data_ptr(), 0, y.data_ptr()) == B.STRATA_EINVAL
     assert B.strata_moe_window_forward(win.handle, x.data_ptr(), 2, x[1].data_ptr()) == B.STRATA_EINVAL
     st, info = B.strata_window_query(win.handle)
-    assert st == B.STRATA_OK and info.n_sm > 0 and info.stages_gateup >= 2
+    assert st == B.STRATA_OK and info.n_sm > 0 and info.stages >= 2 and info.smem_bytes > 0
     assert info.expert_bytes == layer.expert_bytes and info.shared_bytes == layer.shared_bytes
     assert B.strata_window_sync(win.handle) == B.STRATA_OK
