@@ -149,6 +149,31 @@ strata_status strata_window_set_profiling(strata_window* h, int32_t enable);
  * waits for that call.  Returns EINVAL if profiling was never enabled. */
 strata_status strata_window_timings(strata_window* h, float* ms);
 
+/* Size of the one static scratch array that strata_moe_window_forward_noalloc
+ * uses for every window on a device. */
+#define STRATA_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* Run one window like strata_moe_window_forward, but allocate nothing and use
+ * none of the handle's workspace: the window's scratch (router partial logits,
+ * x fragments, gate/up and down results, counters, the grid barrier word)
+ * lives in one file-scope static device array of STRATA_NOALLOC_SCRATCH_BYTES
+ * bytes.  The source pages describe no counterpart of this call; it exists
+ * for callers that may not allocate device memory at call time.
+ *   h: a handle created on the current device (EINVAL otherwise); its
+ *   kernel-ordered weights are read, its error word records device errors
+ *   (reported by strata_window_sync(h)) and its completion event is recorded.
+ *   x, y, T, cuda_stream: as for strata_moe_window_forward; no routing outputs.
+ * The scratch the handle's layer shape needs is computed on the host; above
+ * STRATA_NOALLOC_SCRATCH_BYTES the call returns EUNSUPPORTED and launches
+ * nothing.  The first call on a device looks the array's address up with
+ * cudaGetSymbolAddress while that device is current; make that first call
+ * before any stream capture.  Every call on a device shares the one array: the
+ * parts that must start at zero (the grid barrier word and the x fragments)
+ * are cleared by each call on its stream, and calls that overlap on the GPU
+ * (any handle, any stream) race on the array. */
+strata_status strata_moe_window_forward_noalloc(strata_window* h, const float* x, int32_t T, float* y,
+                                                void* cuda_stream);
+
 /* Free the handle and everything it owns.  NULL is accepted (returns OK). */
 strata_status strata_window_destroy(strata_window* h);
 

@@ -21,7 +21,9 @@ LIB_PATH = os.path.join(PKG, "libstrata_window.so")
 STRATA_OK, STRATA_EINVAL, STRATA_ENOMEM, STRATA_ECUDA, STRATA_EUNSUPPORTED, STRATA_EDEVICE = range(6)
 
 EXPORTED = ("strata_window_create", "strata_moe_window_forward", "strata_window_sync", "strata_window_query",
-            "strata_window_set_profiling", "strata_window_timings", "strata_window_destroy", "strata_status_str")
+            "strata_window_set_profiling", "strata_window_timings", "strata_window_destroy", "strata_status_str",
+            "strata_moe_window_forward_noalloc")
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class StrataError(RuntimeError):
@@ -76,6 +78,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.strata_moe_window_forward.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                               P(strata_routing_out), ctypes.c_void_p]
     lib.strata_moe_window_forward.restype = ctypes.c_int
+    lib.strata_moe_window_forward_noalloc.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                                      ctypes.c_void_p, ctypes.c_void_p]
+    lib.strata_moe_window_forward_noalloc.restype = ctypes.c_int
     lib.strata_window_sync.argtypes = [ctypes.c_void_p]
     lib.strata_window_sync.restype = ctypes.c_int
     lib.strata_window_query.argtypes = [ctypes.c_void_p, P(strata_window_info)]
@@ -113,6 +118,11 @@ def strata_moe_window_forward(handle, x_ptr: int, T: int, y_ptr: int, routing: O
                                             ctypes.c_void_p(y_ptr),
                                             ctypes.byref(routing) if routing is not None else None,
                                             ctypes.c_void_p(stream))
+
+
+def strata_moe_window_forward_noalloc(handle, x_ptr: int, T: int, y_ptr: int, stream: int = 0) -> int:
+    return load().strata_moe_window_forward_noalloc(ctypes.c_void_p(handle), ctypes.c_void_p(x_ptr), T,
+                                                    ctypes.c_void_p(y_ptr), ctypes.c_void_p(stream))
 
 
 def strata_window_sync(handle) -> int:

@@ -3,6 +3,7 @@
 // the persistent window kernel (one cooperative launch, one CTA per SM).
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "common.cuh"
@@ -341,3 +342,98 @@ strata_status strata_window_destroy(strata_window* h) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// the window entry point that allocates nothing: one static scratch array
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) uint8_t g_window_scratch[STRATA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on `dev` (the current device); looked
+// up once per device.
+void* scratch_on(int dev) {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_window_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_scratch_addr[dev] = p;
+  }
+  return g_scratch_addr[dev];
+}
+
+}  // namespace
+
+extern "C" strata_status strata_moe_window_forward_noalloc(strata_window* h, const float* x, int32_t T, float* y,
+                                                           void* cuda_stream) {
+  if (!h || !x || !y) return STRATA_EINVAL;
+  if (T < 1 || T > h->desc.max_rows) return STRATA_EINVAL;
+  const size_t bytes = (size_t)T * h->desc.hidden * sizeof(float);
+  const char* xb = reinterpret_cast<const char*>(x);
+  const char* yb = reinterpret_cast<const char*>(y);
+  if (xb < yb + bytes && yb < xb + bytes) return STRATA_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) % 16 != 0) return STRATA_EINVAL;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return STRATA_ECUDA;
+  }
+  if (dev != h->device || dev < 0 || dev >= kMaxDevices) return STRATA_EINVAL;
+
+  // Scratch layout: the zero-start parts first, so one memset clears them.
+  const int d = h->desc.hidden, E = h->desc.n_experts, F = h->desc.ffn, Fs = h->desc.shared_ffn;
+  const int nmk_d = (d / h->desc.block + 15) / 16;
+  size_t w = 0;
+  const size_t o_gbar = w; w = align_up(w + 8, 256);
+  const size_t o_xf = w; w = align_up(w + (size_t)kMaxRows * frag_halves(d, nmk_d) * 2, 256);
+  const size_t zero_end = w;
+  const size_t o_cnt = w; w = align_up(w + (size_t)(d / 16) * 4, 256);
+  const size_t o_done = w; w = align_up(w + (size_t)(E + 1) * 4, 256);
+  const size_t o_part = w; w = align_up(w + (size_t)h->W.njb * kMaxRows * E * 4, 256);
+  const size_t o_gu = w; w = align_up(w + (size_t)kMaxEntries * F * 8, 256);
+  const size_t o_sgu = w; w = align_up(w + (size_t)kMaxRows * Fs * 8, 256);
+  const size_t o_ob = w; w = align_up(w + (size_t)kMaxEntries * d * 4, 256);
+  const size_t o_sb = w; w = align_up(w + (size_t)kMaxRows * d * 4, 256);
+  if (w > (size_t)STRATA_NOALLOC_SCRATCH_BYTES) return STRATA_EUNSUPPORTED;
+
+  uint8_t* base = static_cast<uint8_t*>(scratch_on(dev));
+  if (!base) return STRATA_ECUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+
+  WindowBufs W = h->W;  // error word and router chunking stay the handle's
+  W.gbar = reinterpret_cast<unsigned long long*>(base + o_gbar);
+  W.xfrag = reinterpret_cast<__half*>(base + o_xf);
+  W.counters = reinterpret_cast<int*>(base + o_cnt);
+  W.done_gu = reinterpret_cast<int*>(base + o_done);
+  W.partial = reinterpret_cast<float*>(base + o_part);
+  W.gu = reinterpret_cast<float2*>(base + o_gu);
+  W.sgu = reinterpret_cast<float2*>(base + o_sgu);
+  W.obuf = reinterpret_cast<float*>(base + o_ob);
+  W.sbuf = reinterpret_cast<float*>(base + o_sb);
+  W.x = x;
+  W.y = y;
+  W.T = T;
+  W.out_topk_idx = nullptr;
+  W.out_topk_w = nullptr;
+  W.out_counts = nullptr;
+  W.out_offsets = nullptr;
+  W.out_entries = nullptr;
+  W.out_distinct = nullptr;
+  W.out_ndistinct = nullptr;
+
+  cudaError_t e = cudaMemsetAsync(base, 0, zero_end, s);
+  if (e == cudaSuccess) e = launch_window(h->L, W, h->cfg, h->nsm, s);
+  if (e == cudaSuccess) e = cudaEventRecord(h->done, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return STRATA_ECUDA;
+  }
+  return STRATA_OK;
+}
