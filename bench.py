@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--sweep-steps", type=int, default=500)
     p.add_argument("--cpu-seconds", type=float, default=20.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-stack", action="store_true", help="skip the 48-layer stack measurement")
+    p.add_argument("--stack-steps", type=int, default=30)
     p.add_argument("--mode", choices=("full", "windows"), default="full",
                    help="windows: only warmup + K windows at --rows (a clean launch sequence for ncu)")
     return p.parse_args()
@@ -387,6 +389,7 @@ def run_ours(args, rank, world, local_rank):
     e2e = {"value": e2e_steps * T * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": T * d * 4,
            "d2h_bytes_per_step": T * d * 4}
 
+    stack = None if args.no_stack else measure_stack(args, dev, flush, stream, peak)
     clocks = sampler.stop()
 
     cpu = None
@@ -408,7 +411,8 @@ def run_ours(args, rank, world, local_rank):
                        "parallelism": "replicas only" if world > 1 else "1 GPU",
                        "arith": "codes -> exact fp16 integers; mma.sync f16 x (fp16 hi + lo activations), fp32 "
                                 "accumulate; fp32 router, softmax, SwiGLU, combine"},
-            "roofline": roofline, "sweep": sweep, "e2e": e2e, "clocks": clocks, "cpu_baseline": cpu,
+            "roofline": roofline, "sweep": sweep, "stack48": stack, "e2e": e2e, "clocks": clocks,
+            "cpu_baseline": cpu,
             "gpu_launches": args.steps,
             "window_us_median": 1e3 * statistics.median(ms), "wall_s_timed_region": wall,
             "handle": {"n_sm": info.n_sm, "stages": info.stages, "stage_bytes": info.stage_bytes,
@@ -416,6 +420,55 @@ def run_ours(args, rank, world, local_rank):
         }
         print(json.dumps(line), flush=True)
     win.close()
+
+
+def measure_stack(args, dev, flush, stream, peak):
+    """The 48-layer decoder stack (dense 4-bit q/k/v/o + the mid MoE per layer),
+    T = 8, one launch per window, L2 flushed before each window."""
+    import numpy as np
+    import torch
+    from slot_decode_window_gb300 import binding, workloads as wlm
+    wl = wlm.WORKLOADS["stack48"]
+    moe = [wlm.make_moe_layer(wl.moe, seed=0, cfg_id=wl.cfg_id, layer=l, device=str(dev)) for l in range(wl.n_layers)]
+    dense = [wlm.make_dense_layer(wl, seed=0, layer=l, device=str(dev)) for l in range(wl.n_layers)]
+    stk = binding.Stack(wl, moe, dense, max_rows=8)
+    del moe, dense
+    torch.cuda.empty_cache()
+    info = stk.info()
+    T, nw = 8, 8
+    X = torch.from_numpy(np.stack([wlm.make_window(wl, T, seed=0, window=w) for w in range(nw)])).to(dev)
+    Y = torch.empty(T, wl.moe.hidden, device=dev)
+    per_window = []
+    for w in range(nw):
+        _, res = stk.forward(X[w], Y, outputs=True)
+        ndl = res["n_distinct"].cpu().numpy()
+        per_window.append(float(ndl.sum() * info.expert_bytes
+                                + wl.n_layers * (info.shared_bytes + info.router_bytes + info.dense_bytes)
+                                + 2 * T * wl.moe.hidden * 4))
+    stk.sync()
+    steps, warm = args.stack_steps, 3
+    for i in range(warm):
+        stk.forward(X[i % nw], Y)
+    stk.set_profiling(True)
+    ms = []
+    nbytes = 0.0
+    for i in range(steps):
+        flush.zero_()
+        stk.forward(X[i % nw], Y)
+        ms.append(stk.timings())
+        nbytes += per_window[i % nw]
+    stk.set_profiling(False)
+    stk.sync()
+    tot = sum(ms) / 1e3
+    achieved = nbytes / tot / 1e9
+    out = {"workload": "48 layers x (RMSNorm, dense 4-bit q/k/v/o 2048->4096/512/512, o 4096->2048, "
+                       "MoE d2048 E128 k8 F768 + shared 768), T=8",
+           "windows": steps, "warmup": warm, "ms_per_window_median": statistics.median(ms),
+           "rows_per_s": steps * T / tot, "algorithmic_bytes_per_window": nbytes / steps,
+           "achieved_GBps": achieved, "peak_GBps": peak, "frac": achieved / peak,
+           "kernel": "stack_kernel<4> (one cooperative launch per window)", "gpu_launches_per_window": 1}
+    stk.close()
+    return out
 
 
 def main():

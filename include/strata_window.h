@@ -149,6 +149,79 @@ strata_status strata_window_set_profiling(strata_window* h, int32_t enable);
  * waits for that call.  Returns EINVAL if profiling was never enabled. */
 strata_status strata_window_timings(strata_window* h, float* ms);
 
+/* ---------------------------------------------------------------------------
+ * A window through a stack of decoder layers.
+ *
+ * Each layer: a = RMSNorm(x); q = Wq a, k = Wk a, v = Wv a; attention over a
+ * context of one position, so query head h outputs v of kv head
+ * h / (heads / kv_heads); x1 = x + Wo att; x_next = x1 + MoE(RMSNorm(x1)).
+ * RMSNorm(x) = x / sqrt(mean(x^2) + 1e-6) with unit gain.  The Strata docs
+ * ("BATCHING.md", "Several requests at once (batch slots)", opening
+ * paragraph) name the dense weights among what a window reads once for all of
+ * its rows; the pages give no attention or norm formulas, so these are the
+ * plain readings (pre-norm, residual adds, no final norm).
+ * ------------------------------------------------------------------------- */
+typedef struct strata_stack strata_stack;
+
+/* Dense attention shapes; the weights use the MoE desc's bits/block format.
+ * heads % kv_heads == 0, (heads / kv_heads) and (head_dim / k-step) powers of
+ * two, head_dim a multiple of the k-step (64 for 4-bit, 128 for 2-bit). */
+typedef struct {
+  int32_t heads, kv_heads, head_dim;
+} strata_attn_desc;
+
+typedef struct {
+  strata_qmat q;  /* [heads*head_dim][hidden] */
+  strata_qmat k;  /* [kv_heads*head_dim][hidden] */
+  strata_qmat v;  /* [kv_heads*head_dim][hidden] */
+  strata_qmat o;  /* [hidden][heads*head_dim] */
+} strata_attn_weights;
+
+/* Optional per-layer outputs of a stack window (device pointers, each may be NULL). */
+typedef struct {
+  float* q;              /* [n_layers][T][heads*head_dim] */
+  float* k;              /* [n_layers][T][kv_heads*head_dim] */
+  int32_t* topk_idx;     /* [n_layers][T][top_k] */
+  float* topk_w;         /* [n_layers][T][top_k] */
+  int32_t* n_distinct;   /* [n_layers] */
+} strata_stack_out;
+
+typedef struct {
+  int32_t n_layers;
+  int32_t n_sm, stages, stage_bytes, smem_bytes;
+  int64_t dense_bytes;   /* block-format bytes of one layer's q, k, v, o */
+  int64_t expert_bytes;  /* per routed expert, as strata_window_info */
+  int64_t shared_bytes;
+  int64_t router_bytes;
+} strata_stack_info;
+
+/* Create a stack of n_layers decoder layers, all with the shapes of `moe` and
+ * `attn`; moe_w and attn_w point to n_layers weight sets (borrowed for the
+ * duration of the call: the handle keeps its own kernel-ordered copies).
+ * Returns EINVAL (bad pointer or shape), EUNSUPPORTED, ENOMEM, ECUDA. */
+strata_status strata_stack_create(int32_t n_layers, const strata_moe_desc* moe, const strata_attn_desc* attn,
+                                  const strata_moe_weights* moe_w, const strata_attn_weights* attn_w,
+                                  void* cuda_stream, strata_stack** out);
+
+/* Run one window of T rows through every layer: x device fp32 [T][hidden]
+ * (caller-owned, 16-byte aligned), y device fp32 [T][hidden] (must not
+ * overlap x, 16-byte aligned); out may be NULL.  One cooperative launch,
+ * asynchronous on cuda_stream. */
+strata_status strata_stack_forward(strata_stack* s, const float* x, int32_t T, float* y, const strata_stack_out* out,
+                                   void* cuda_stream);
+
+/* Wait for the last stack_forward; EDEVICE if the GPU recorded an error. */
+strata_status strata_stack_sync(strata_stack* s);
+
+strata_status strata_stack_query(const strata_stack* s, strata_stack_info* info);
+
+/* Measurement aid, as strata_window_set_profiling / strata_window_timings. */
+strata_status strata_stack_set_profiling(strata_stack* s, int32_t enable);
+strata_status strata_stack_timings(strata_stack* s, float* ms);
+
+/* Free the stack and everything it owns.  NULL is accepted. */
+strata_status strata_stack_destroy(strata_stack* s);
+
 /* Size of the one static scratch array that strata_moe_window_forward_noalloc
  * uses for every window on a device. */
 #define STRATA_NOALLOC_SCRATCH_BYTES (4u << 20)

@@ -260,10 +260,12 @@ def dense_attention_len1(v: np.ndarray, heads: int, kv_heads: int, head_dim: int
     return np.concatenate([vh[h // group] for h in range(heads)])
 
 
-def decoder_layer_row(x: np.ndarray, dense: ODenseLayer, moe: OMoELayer):
+def decoder_layer_row(x: np.ndarray, dense: ODenseLayer, moe: OMoELayer, trace: Optional[dict] = None):
     """One decoder layer on one row: pre-norm attention + residual, pre-norm MoE + residual.
 
-    Returns (x_out, q, k, routing (selected, gates)).
+    Returns (x_out, q, k, routing (selected, gates)).  ``trace``, if given,
+    receives ``x1`` (the residual stream after attention) and ``margin`` (the
+    router's top-k logit margin on ``rmsnorm(x1)``).
     """
     a = rmsnorm(x)
     q = dequant(dense.q) @ a
@@ -271,7 +273,11 @@ def decoder_layer_row(x: np.ndarray, dense: ODenseLayer, moe: OMoELayer):
     v = dequant(dense.v) @ a
     att = dense_attention_len1(v, dense.heads, dense.kv_heads, dense.head_dim)
     x1 = x.astype(np.float64) + dequant(dense.o) @ att
-    y, sel, g = moe_row(rmsnorm(x1), moe)
+    b = rmsnorm(x1)
+    y, sel, g = moe_row(b, moe)
+    if trace is not None:
+        trace["x1"] = x1
+        trace["margin"] = topk_margin(b, moe.router_w, moe.router_b, moe.top_k)
     return x1 + y, q, kk, (sel, g)
 
 

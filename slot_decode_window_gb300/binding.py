@@ -22,7 +22,8 @@ STRATA_OK, STRATA_EINVAL, STRATA_ENOMEM, STRATA_ECUDA, STRATA_EUNSUPPORTED, STRA
 
 EXPORTED = ("strata_window_create", "strata_moe_window_forward", "strata_window_sync", "strata_window_query",
             "strata_window_set_profiling", "strata_window_timings", "strata_window_destroy", "strata_status_str",
-            "strata_moe_window_forward_noalloc")
+            "strata_moe_window_forward_noalloc", "strata_stack_create", "strata_stack_forward", "strata_stack_sync",
+            "strata_stack_query", "strata_stack_set_profiling", "strata_stack_timings", "strata_stack_destroy")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -59,6 +60,24 @@ class strata_window_info(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_int64)]
 
 
+class strata_attn_desc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("heads", "kv_heads", "head_dim")]
+
+
+class strata_attn_weights(ctypes.Structure):
+    _fields_ = [("q", strata_qmat), ("k", strata_qmat), ("v", strata_qmat), ("o", strata_qmat)]
+
+
+class strata_stack_out(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "topk_idx", "topk_w", "n_distinct")]
+
+
+class strata_stack_info(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("n_sm", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("stage_bytes", ctypes.c_int32), ("smem_bytes", ctypes.c_int32), ("dense_bytes", ctypes.c_int64),
+                ("expert_bytes", ctypes.c_int64), ("shared_bytes", ctypes.c_int64), ("router_bytes", ctypes.c_int64)]
+
+
 _lib: Optional[ctypes.CDLL] = None
 
 
@@ -81,6 +100,23 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.strata_moe_window_forward_noalloc.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                                       ctypes.c_void_p, ctypes.c_void_p]
     lib.strata_moe_window_forward_noalloc.restype = ctypes.c_int
+    lib.strata_stack_create.argtypes = [ctypes.c_int32, P(strata_moe_desc), P(strata_attn_desc),
+                                        P(strata_moe_weights), P(strata_attn_weights), ctypes.c_void_p,
+                                        P(ctypes.c_void_p)]
+    lib.strata_stack_create.restype = ctypes.c_int
+    lib.strata_stack_forward.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                         P(strata_stack_out), ctypes.c_void_p]
+    lib.strata_stack_forward.restype = ctypes.c_int
+    lib.strata_stack_sync.argtypes = [ctypes.c_void_p]
+    lib.strata_stack_sync.restype = ctypes.c_int
+    lib.strata_stack_query.argtypes = [ctypes.c_void_p, P(strata_stack_info)]
+    lib.strata_stack_query.restype = ctypes.c_int
+    lib.strata_stack_set_profiling.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+    lib.strata_stack_set_profiling.restype = ctypes.c_int
+    lib.strata_stack_timings.argtypes = [ctypes.c_void_p, P(ctypes.c_float)]
+    lib.strata_stack_timings.restype = ctypes.c_int
+    lib.strata_stack_destroy.argtypes = [ctypes.c_void_p]
+    lib.strata_stack_destroy.restype = ctypes.c_int
     lib.strata_window_sync.argtypes = [ctypes.c_void_p]
     lib.strata_window_sync.restype = ctypes.c_int
     lib.strata_window_query.argtypes = [ctypes.c_void_p, P(strata_window_info)]
@@ -123,6 +159,45 @@ def strata_moe_window_forward(handle, x_ptr: int, T: int, y_ptr: int, routing: O
 def strata_moe_window_forward_noalloc(handle, x_ptr: int, T: int, y_ptr: int, stream: int = 0) -> int:
     return load().strata_moe_window_forward_noalloc(ctypes.c_void_p(handle), ctypes.c_void_p(x_ptr), T,
                                                     ctypes.c_void_p(y_ptr), ctypes.c_void_p(stream))
+
+
+def strata_stack_create(n_layers: int, desc: strata_moe_desc, attn: strata_attn_desc, moe_w, attn_w,
+                        stream: int = 0):
+    """moe_w / attn_w: ctypes arrays of n_layers weight structs.  Returns (status, handle or None)."""
+    h = ctypes.c_void_p()
+    st = load().strata_stack_create(n_layers, ctypes.byref(desc), ctypes.byref(attn), moe_w, attn_w,
+                                    ctypes.c_void_p(stream), ctypes.byref(h))
+    return st, (h.value if st == STRATA_OK else None)
+
+
+def strata_stack_forward(handle, x_ptr: int, T: int, y_ptr: int, out: Optional[strata_stack_out] = None,
+                         stream: int = 0) -> int:
+    return load().strata_stack_forward(ctypes.c_void_p(handle), ctypes.c_void_p(x_ptr), T, ctypes.c_void_p(y_ptr),
+                                       ctypes.byref(out) if out is not None else None, ctypes.c_void_p(stream))
+
+
+def strata_stack_sync(handle) -> int:
+    return load().strata_stack_sync(ctypes.c_void_p(handle))
+
+
+def strata_stack_query(handle):
+    info = strata_stack_info()
+    st = load().strata_stack_query(ctypes.c_void_p(handle), ctypes.byref(info))
+    return st, info
+
+
+def strata_stack_set_profiling(handle, enable: bool) -> int:
+    return load().strata_stack_set_profiling(ctypes.c_void_p(handle), 1 if enable else 0)
+
+
+def strata_stack_timings(handle):
+    ms = ctypes.c_float()
+    st = load().strata_stack_timings(ctypes.c_void_p(handle), ctypes.byref(ms))
+    return st, ms.value
+
+
+def strata_stack_destroy(handle) -> int:
+    return load().strata_stack_destroy(ctypes.c_void_p(handle))
 
 
 def strata_window_sync(handle) -> int:
@@ -235,6 +310,84 @@ class Window:
     def close(self) -> None:
         if getattr(self, "handle", None):
             strata_window_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def attn_desc_of(wl) -> strata_attn_desc:
+    return strata_attn_desc(wl.heads, wl.kv_heads, wl.head_dim)
+
+
+def attn_weights_of(dl) -> strata_attn_weights:
+    return strata_attn_weights(_qmat(dl.q), _qmat(dl.k), _qmat(dl.v), _qmat(dl.o))
+
+
+class Stack:
+    """A handle for a stack of decoder layers whose weights are CUDA torch tensors.
+
+    moe_layers / dense_layers: per-layer ``workloads.MoELayer`` / ``DenseLayer``;
+    wl: the workload (attention shapes).  The handle keeps its own
+    kernel-ordered copies, so the tensors may be freed after construction.
+    """
+
+    def __init__(self, wl, moe_layers, dense_layers, max_rows: int = 8, stream=None):
+        import torch
+        n = len(moe_layers)
+        assert n == len(dense_layers) and n >= 1
+        self.wl, self.n_layers, self.spec = wl, n, moe_layers[0].spec
+        mw = (strata_moe_weights * n)(*[weights_of(m) for m in moe_layers])
+        aw = (strata_attn_weights * n)(*[attn_weights_of(dl) for dl in dense_layers])
+        s = (stream or torch.cuda.current_stream()).cuda_stream
+        st, h = strata_stack_create(n, desc_of(self.spec, max_rows), attn_desc_of(wl), mw, aw, s)
+        check(st, "strata_stack_create")
+        self.handle = h
+
+    def info(self) -> strata_stack_info:
+        st, info = strata_stack_query(self.handle)
+        check(st, "strata_stack_query")
+        return info
+
+    def forward(self, x, y=None, outputs: bool = False, stream=None):
+        """Enqueue one window on x [T][d]; returns y (and per-layer q, k, routing)."""
+        import torch
+        assert x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()
+        T, d = x.shape
+        if y is None:
+            y = torch.empty_like(x)
+        o = None
+        res = None
+        if outputs:
+            n, wl, k = self.n_layers, self.wl, self.spec.top_k
+            dev = x.device
+            res = dict(q=torch.empty(n, T, wl.heads * wl.head_dim, device=dev),
+                       k=torch.empty(n, T, wl.kv_heads * wl.head_dim, device=dev),
+                       topk_idx=torch.empty(n, T, k, dtype=torch.int32, device=dev),
+                       topk_w=torch.empty(n, T, k, device=dev),
+                       n_distinct=torch.empty(n, dtype=torch.int32, device=dev))
+            o = strata_stack_out(*(res[m].data_ptr() for m in ("q", "k", "topk_idx", "topk_w", "n_distinct")))
+        s = (stream or torch.cuda.current_stream()).cuda_stream
+        check(strata_stack_forward(self.handle, x.data_ptr(), T, y.data_ptr(), o, s), "strata_stack_forward")
+        return (y, res) if outputs else y
+
+    def set_profiling(self, enable: bool) -> None:
+        check(strata_stack_set_profiling(self.handle, enable), "strata_stack_set_profiling")
+
+    def timings(self):
+        st, ms = strata_stack_timings(self.handle)
+        check(st, "strata_stack_timings")
+        return ms
+
+    def sync(self) -> None:
+        check(strata_stack_sync(self.handle), "strata_stack_sync")
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            strata_stack_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

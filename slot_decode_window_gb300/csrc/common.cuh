@@ -81,6 +81,11 @@ struct LayerDev {
   const float* router_w;   // [E][d]
   const float* router_b;   // [E] or null
   PackedMat gate, up, down, sgate, sup, sdown;
+  // dense attention projections of a decoder layer (stack kernel only):
+  // qkv = [Wq; Wk; Wv] as one [dq + 2 dkv][d] matrix, o = Wo [d][dq]
+  PackedMat qkv, o;
+  int dq, dkv;             // query width (heads x head_dim) and kv width
+  int kph_log2, kpg_log2;  // log2 of the o-projection k-steps per head / per kv group
 };
 
 struct WindowBufs {
@@ -102,11 +107,19 @@ struct WindowBufs {
   float* partial;          // router partial logits [njb][kMaxRows][E]
   int njb;                 // column chunks of the router GEMV
   unsigned* err;
+  // decoder-layer extras (stack kernel only; null in the single-layer kernel)
+  const float* rinv;       // [T] 1 / RMS of each row of x (inputs are x * rinv)
+  const float* resid;      // [T][d] added to y in the combine
+  float* v;                // [kMaxRows][dkv] value projection
+  float* x1;               // [kMaxRows][d] x + Wo att
+  float* q_out;            // [T][dq] or null
+  float* k_out;            // [T][dkv] or null
 };
 
 constexpr int kMaxChunks = 32;  // k-chunks per tile
 
-// How one phase (0 gate/up, 1 down) cuts its tiles into ring stages.
+// How one phase (0 gate/up, 1 down, 2 dense q/k/v, 3 dense o) cuts its tiles
+// into ring stages.
 struct PhaseCfg {
   int nchunks;             // k-chunks per tile
   int sub_stride;          // bytes per sub-tile inside a stage
@@ -124,7 +137,7 @@ struct KernelCfg {
   int bsum_halves;         // B sums halves per set: nmk_max*8*4*4
   int nsets;               // 1 (rows <= 4) or 2
   int total_bytes;
-  PhaseCfg ph[2];
+  PhaseCfg ph[4];
 };
 
 // ---------------------------------------------------------------------------

@@ -1,0 +1,26 @@
+// Internal: the window handle, shared by the window and stack entry points.
+#pragma once
+#include "common.cuh"
+#include "strata_window.h"
+
+struct strata_window {
+  strata_moe_desc desc;
+  int device = 0;
+  int nsm = 0;
+  strata::LayerDev L{};
+  strata::WindowBufs W{};
+  strata::KernelCfg cfg{};
+  float* partial = nullptr;
+  void* wmem = nullptr;
+  void* ws = nullptr;
+  long long packed = 0, ws_bytes = 0;
+  cudaEvent_t done = nullptr;
+  bool profiling = false;
+  bool profiled_once = false;
+  cudaEvent_t prof[2] = {nullptr, nullptr};
+};
+
+namespace strata {
+// The STRATA_FAULT test hook: true when the environment names `what`.
+bool fault_is(const char* what);
+}  // namespace strata

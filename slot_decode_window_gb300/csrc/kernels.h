@@ -14,6 +14,14 @@ int window_blocks_per_sm(int bits, int smem_bytes);
 // One window: router, grouping, gate/up, down and combine in one cooperative launch.
 cudaError_t launch_window(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, int grid, cudaStream_t s);
 
+// A window through n decoder layers (dense q/k/v/o + MoE) in one cooperative
+// launch; layers is a device array of n LayerDev.
+cudaError_t stack_set_attrs(int bits, int smem_bytes);
+int stack_blocks_per_sm(int bits, int smem_bytes);
+cudaError_t launch_stack(const LayerDev* layers, int n_layers, int bits, const WindowBufs& W, const KernelCfg& C,
+                         int grid, const float* x, float* y, float* ybuf, float* q_all, float* k_all,
+                         cudaStream_t s);
+
 // Repack one canonical block-quantized matrix stack into the tile format.
 cudaError_t launch_repack(const uint8_t* codes, const uint16_t* scale, const uint16_t* mn, int n, int rows, int K,
                           int bits, uint8_t* out, cudaStream_t s);

@@ -7,34 +7,18 @@
 #include <new>
 
 #include "common.cuh"
+#include "handle.h"
 #include "kernels.h"
 #include "strata_window.h"
 
 using namespace strata;
 
-struct strata_window {
-  strata_moe_desc desc;
-  int device = 0;
-  int nsm = 0;
-  LayerDev L{};
-  WindowBufs W{};
-  KernelCfg cfg{};
-  float* partial = nullptr;
-  void* wmem = nullptr;
-  void* ws = nullptr;
-  long long packed = 0, ws_bytes = 0;
-  cudaEvent_t done = nullptr;
-  bool profiling = false;
-  bool profiled_once = false;
-  cudaEvent_t prof[2] = {nullptr, nullptr};
-};
-
-namespace {
-
-bool fault_is(const char* what) {
+bool strata::fault_is(const char* what) {
   const char* f = std::getenv("STRATA_FAULT");
   return f && std::strcmp(f, what) == 0;
 }
+
+namespace {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

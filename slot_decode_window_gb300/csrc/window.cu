@@ -169,16 +169,23 @@ __device__ __forceinline__ void kstep_mma(const uint8_t* __restrict__ ch, const 
 // This warp's share of one staged chunk of its sub-tile: k-steps [k0, k1)
 // (chunk-local, tile k-step ks_base + kl) and min groups [m0, m1) (chunk-local,
 // tile group mk_base + ml).
-template <int BITS, bool PAIRED>
+// VMAP: the activation is the grouped-query broadcast of v, so k-step ks of
+// the 4096-wide input reads v's k-step (ks >> kpg) * 2^kph + (ks & (2^kph - 1))
+// (kph, kpg: log2 of k-steps per head and per kv group).
+template <int BITS, bool PAIRED, bool VMAP = false>
 __device__ __forceinline__ void chunk_mma(const uint8_t* __restrict__ sub, int mins_off, int ks_base, int k0, int k1,
                                           int mk_base, int m0, int m1, const __half* __restrict__ bm,
                                           const __half* __restrict__ bs, int bm_set, int bs_set, bool bon, int lane,
-                                          float (&acc)[4], float (&accm)[4]) {
+                                          float (&acc)[4], float (&accm)[4], int kph = 0, int kpg = 0) {
   constexpr int S = Fmt<BITS>::kBHalves;
   const uint8_t* a = sub + k0 * Fmt<BITS>::kChunk;
   const __half* bk = bm + (ks_base + k0) * 32 * S + lane * 8;
 #pragma unroll 2
   for (int kl = k0; kl < k1; ++kl) {
+    if constexpr (VMAP) {
+      const int ks = ks_base + kl;
+      bk = bm + (((ks >> kpg) << kph) + (ks & ((1 << kph) - 1))) * 32 * S + lane * 8;
+    }
     kstep_mma<BITS, PAIRED>(a, bk, bm_set, bon, lane, acc);
     a += Fmt<BITS>::kChunk;
     bk += 32 * S;
@@ -221,7 +228,7 @@ struct SPlan {
   int finish[kMaxEntries * 4];      // row slices this CTA combines
   int nfinish;
   int ok;                           // the grid barrier passed
-  PhaseTasks pt[2];
+  PhaseTasks pt[4];                 // gate/up, down, dense q/k/v, dense o
 };
 
 __device__ __forceinline__ unsigned ord_f32(float f) {
@@ -249,7 +256,7 @@ __device__ void write_x_frags(const LayerDev& L, const WindowBufs& W) {
     const long long i = tid + it * stride;
     const bool in = i < n_el;
     const int t = in ? (int)(i / d) : 0, j = in ? (int)(i % d) : 0;
-    const float v = in ? W.x[i] : 0.f;
+    const float v = in ? (W.rinv ? W.x[i] * W.rinv[t] : W.x[i]) : 0.f;
     __half* base = W.xfrag + t * fh;
     if (in) {
       int off;
@@ -271,6 +278,34 @@ __device__ void write_x_frags(const LayerDev& L, const WindowBufs& W) {
       base[2 * d + nmk * 16 + off] = lo;
     }
   }
+}
+
+// 1 / sqrt(mean(x_t^2) + 1e-6) of every row (warp t sums row t in a fixed
+// order, so every CTA gets the same bits).  Ends with a block barrier.
+__device__ __noinline__ void row_rinv(const float* x, int T, int d, float* s_rinv) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < T) {
+    const float4* xr = reinterpret_cast<const float4*>(x + (long long)warp * d);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j0 = 0; j0 < d / 4; j0 += 128) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * 32 + lane;
+        if (j < d / 4) {
+          const float4 v = __ldcg(xr + j);
+          acc[u] = fmaf(v.x, v.x, acc[u]);
+          acc[u] = fmaf(v.y, v.y, acc[u]);
+          acc[u] = fmaf(v.z, v.z, acc[u]);
+          acc[u] = fmaf(v.w, v.w, acc[u]);
+        }
+      }
+    }
+    float ss = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) s_rinv[warp] = 1.0f / sqrtf(ss / (float)d + 1e-6f);
+  }
+  __syncthreads();
 }
 
 template <int BITS>
@@ -304,7 +339,7 @@ __device__ __noinline__ void router_stage(const LayerDev& L, const WindowBufs& W
       float v = acc[t];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == t && t < T) W.partial[((long long)jb * kMaxRows + t) * E + e] = v;
+      if (lane == t && t < T) W.partial[((long long)jb * kMaxRows + t) * E + e] = W.rinv ? v * W.rinv[t] : v;
     }
   }
   write_x_frags<BITS>(L, W);
@@ -576,7 +611,7 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
   const int nks = K / Fmt<BITS>::kKstep;
   const int nmk = (K / B + 15) / 16;
   const bool paired = R <= 4;
-  if (PHASE == 0) {
+  if (PHASE == 0 || PHASE == 2) {
     const long long fh = frag_halves(K, nmk);
     const int nsets = paired ? 1 : 2;
     const int ncols = paired ? 2 * R : R;
@@ -587,7 +622,7 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
       const int set = cs / ncols, col = cs - set * ncols;
       const int r = paired ? (col >> 1) : col;
       const int part = paired ? (col & 1) : set;
-      const int xrow = is_shared ? r : sp.entries[ent_off + r] / L.k;
+      const int xrow = (PHASE == 2 || is_shared) ? r : sp.entries[ent_off + r] / L.k;
       const int ks = rem / (4 * (S / 8)), cp = rem - ks * 4 * (S / 8);
       const int c = cp / (S / 8), p = cp - c * (S / 8);
       const uint4 v = __ldcg(reinterpret_cast<const uint4*>(W.xfrag + xrow * fh + (long long)part * K + ks * 4 * S +
@@ -600,7 +635,7 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
       const int set = cs / ncols, col = cs - set * ncols;
       const int r = paired ? (col >> 1) : col;
       const int part = paired ? (col & 1) : set;
-      const int xrow = is_shared ? r : sp.entries[ent_off + r] / L.k;
+      const int xrow = (PHASE == 2 || is_shared) ? r : sp.entries[ent_off + r] / L.k;
       const int mk = rem >> 2, c = rem & 3;
       const uint2 v = __ldcg(reinterpret_cast<const uint2*>(W.xfrag + xrow * fh + 2LL * K +
                                                             (long long)part * 16 * nmk + mk * 16 + c * 4));
@@ -608,16 +643,23 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
     }
   } else {
     // one element per thread and step; a warp covers 32 consecutive elements of
-    // one row (K is a multiple of 64), so block sums come from lane shuffles
+    // one row (K is a multiple of 64), so block sums come from lane shuffles.
+    // Phase 1: h = silu(gu) * uu.  Phase 3: h = v (K = dkv); its block sums are
+    // written for every block of the broadcast input that repeats that v block.
     for (int i0 = 0; i0 < R * K; i0 += kConsumerThreads) {
       const int i = i0 + ctid;
       const bool in = i < R * K;
       const int r = in ? i / K : 0, f = in ? i - r * K : 0;
       float h = 0.f;
       if (in) {
-        const float2* src = is_shared ? W.sgu + (long long)r * L.Fs : W.gu + (long long)sp.entries[ent_off + r] * L.F;
-        const float2 gu = __ldcg(src + f);
-        h = silu_f32(gu.x) * gu.y;
+        if constexpr (PHASE == 3) {
+          h = __ldcg(W.v + (long long)r * L.dkv + f);
+        } else {
+          const float2* src =
+              is_shared ? W.sgu + (long long)r * L.Fs : W.gu + (long long)sp.entries[ent_off + r] * L.F;
+          const float2 gu = __ldcg(src + f);
+          h = silu_f32(gu.x) * gu.y;
+        }
         int off;
         float fac;
         frag_main_pos<BITS>(f, off, fac);
@@ -637,17 +679,24 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
 #pragma unroll
       for (int o = B / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
       if (in && (f % B) == 0) {
-        const int spos = frag_sum_pos(f / B);
-        const int mk = spos >> 4, c = (spos >> 2) & 3, slot = spos & 3;
         __half hi, lo;
         split_hi_lo(s, hi, lo);
-        const int o = mk * 128 + c * 4 + slot;
-        if (paired) {
-          bs[o + (2 * r) * 16] = hi;
-          bs[o + (2 * r + 1) * 16] = lo;
-        } else {
-          bs[o + r * 16] = hi;
-          bs[C.bsum_halves + o + r * 16] = lo;
+        // v block vb = (kv group, block in head) -> broadcast blocks (group * G + head) * bph + j
+        const int bph = PHASE == 3 ? (1 << L.kph_log2) * Fmt<BITS>::kBlocksPerKstep : 1;
+        const int ncopy = PHASE == 3 ? 1 << (L.kpg_log2 - L.kph_log2) : 1;
+        const int vb = f / B, grp = vb / bph, j = vb - grp * bph;
+        for (int hc = 0; hc < ncopy; ++hc) {
+          const int beta = PHASE == 3 ? (grp * ncopy + hc) * bph + j : vb;
+          const int spos = frag_sum_pos(beta);
+          const int mk = spos >> 4, c = (spos >> 2) & 3, slot = spos & 3;
+          const int o = mk * 128 + c * 4 + slot;
+          if (paired) {
+            bs[o + (2 * r) * 16] = hi;
+            bs[o + (2 * r + 1) * 16] = lo;
+          } else {
+            bs[o + r * 16] = hi;
+            bs[C.bsum_halves + o + r * 16] = lo;
+          }
         }
       }
     }
@@ -723,7 +772,7 @@ __device__ bool produce(const LayerDev& L, const WindowBufs& W, const KernelCfg&
       *rg.abort_flag = 1;
       return false;
     }
-    const int K = PHASE == 0 ? L.d : (tk.shared ? L.Fs : L.F);
+    const int K = PHASE == 0 ? L.d : PHASE == 1 ? (tk.shared ? L.Fs : L.F) : PHASE == 2 ? L.d : L.dq;
     const int nks = K / Fmt<BITS>::kKstep, nmk = (K / Fmt<BITS>::kBlock + 15) / 16;
     const int tbytes = nks * Fmt<BITS>::kChunk + nmk * 512;
     const int kv = (PHASE == 1 && tk.shared) ? 1 : 0;
@@ -738,8 +787,10 @@ __device__ bool produce(const LayerDev& L, const WindowBufs& W, const KernelCfg&
 #pragma unroll
       for (int s = 0; s < NS; ++s) {
         const bool up = PHASE == 0 && s >= kMT;
-        const PackedMat& M = PHASE == 0 ? (up ? (tk.shared ? L.sup : L.up) : (tk.shared ? L.sgate : L.gate))
-                                        : (tk.shared ? L.sdown : L.down);
+        const PackedMat& M = PHASE == 0   ? (up ? (tk.shared ? L.sup : L.up) : (tk.shared ? L.sgate : L.gate))
+                             : PHASE == 1 ? (tk.shared ? L.sdown : L.down)
+                             : PHASE == 2 ? L.qkv
+                                          : L.o;
         const int tile = tk.tile + (up ? s - kMT : s);
         const uint8_t* src =
             M.base + (tk.shared ? 0LL : (long long)tk.expert * M.mat_bytes) + (long long)tile * tbytes;
@@ -784,7 +835,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
   for (int task = pt.t0; task < pt.t1; ++task, tw.next(pt, has_shared, sp)) {
     const Task& tk = tw.tk;
     if (!tk.shared && (unsigned)tk.expert >= (unsigned)L.E) break;  // flagged by the producer
-    const int K = PHASE == 0 ? L.d : (tk.shared ? L.Fs : L.F);
+    const int K = PHASE == 0 ? L.d : PHASE == 1 ? (tk.shared ? L.Fs : L.F) : PHASE == 2 ? L.d : L.dq;
     if (tk.group != cur) {
       if (tk.shared) {
         R = W.T;
@@ -817,7 +868,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
         consumer_sync();
       }
       // the previous task's barrier guarantees no warp still reads the old fragments
-      load_group_B<BITS, PHASE>(L, W, sp, C, bm, bs, tk.shared, R, ent_off, K, tid);
+      load_group_B<BITS, PHASE>(L, W, sp, C, bm, bs, tk.shared, R, ent_off, PHASE == 3 ? L.dkv : K, tid);
       consumer_sync();
       cur = tk.group;
     }
@@ -832,12 +883,13 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
       const int stage = rp.stage;
       if (wait_bar(&rg.full[stage], rp.parity, W.err, rg.abort_flag)) {
         const uint8_t* st = rg.base + (size_t)stage * C.stage_bytes + sub * P.sub_stride;
+        constexpr bool kVmap = PHASE == 3;
         if (paired)
-          chunk_mma<BITS, true>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves, C.bsum_halves,
-                                bon, lane, acc, accm);
+          chunk_mma<BITS, true, kVmap>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
+                                       C.bsum_halves, bon, lane, acc, accm, L.kph_log2, L.kpg_log2);
         else
-          chunk_mma<BITS, false>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves, C.bsum_halves,
-                                 bon, lane, acc, accm);
+          chunk_mma<BITS, false, kVmap>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
+                                        C.bsum_halves, bon, lane, acc, accm, L.kph_log2, L.kpg_log2);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&rg.empty[stage]);
@@ -876,7 +928,18 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
 #pragma unroll
         for (int w = 0; w < kWPS; ++w) v += frag_pick(rb[(s * kWPS + w) * 32 + src_lane], idx, paired);
         const int drow = (tk.tile + s) * 16 + row;
-        if (tk.shared) {
+        if constexpr (PHASE == 2) {
+          // rows of [Wq; Wk; Wv]
+          if (drow < L.dq) {
+            if (W.q_out) W.q_out[(long long)r * L.dq + drow] = v;
+          } else if (drow < L.dq + L.dkv) {
+            if (W.k_out) W.k_out[(long long)r * L.dkv + drow - L.dq] = v;
+          } else {
+            W.v[(long long)r * L.dkv + drow - L.dq - L.dkv] = v;
+          }
+        } else if constexpr (PHASE == 3) {
+          W.x1[(long long)r * L.d + drow] = W.x[(long long)r * L.d + drow] + v;
+        } else if (tk.shared) {
           W.sbuf[(long long)r * L.d + drow] = v;
         } else {
           const int ent = sp.entries[ent_off + r];
@@ -916,6 +979,13 @@ __device__ void combine(const LayerDev& L, const WindowBufs& W, SPlan& sp) {
     const int t = u >> 2, rr = tile * 16 + (u & 3) * 4;
     float4 y = has_shared ? __ldcg(reinterpret_cast<const float4*>(W.sbuf + (long long)t * L.d + rr))
                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (W.resid) {
+      const float4 x1 = __ldcg(reinterpret_cast<const float4*>(W.resid + (long long)t * L.d + rr));
+      y.x += x1.x;
+      y.y += x1.y;
+      y.z += x1.z;
+      y.w += x1.w;
+    }
     float4 o[kMaxTopK];
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j)
@@ -951,46 +1021,64 @@ __device__ void combine(const LayerDev& L, const WindowBufs& W, SPlan& sp) {
   for (int i = tid; i < nf * W.T * 4; i += kConsumerThreads) sum_quad(sp.finish[i / (W.T * 4)], i % (W.T * 4));
 }
 
-}  // namespace
-
-// Shared memory: [ring: nstages x stage_bytes][B main: nsets][B sums: nsets]
-// [red: 2 x 16 warps x 32 lanes float4][full/empty mbarriers]; static: SPlan.
-template <int BITS>
-__global__ void __launch_bounds__(kExpertThreads, 1) window_kernel(LayerDev L, WindowBufs W, KernelCfg C) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ volatile int s_abort;
-  __shared__ SPlan sp;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  uint8_t* ring = smem;
-  __half* bm = reinterpret_cast<__half*>(smem + (size_t)C.nstages * C.stage_bytes);
-  __half* bs = bm + (size_t)C.nsets * C.bmain_halves;
-  float4* red = reinterpret_cast<float4*>(bs + (size_t)C.nsets * C.bsum_halves);
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * kConsumerWarps * 32);
-  uint64_t* empty = full + kMaxStages;
-  const Ring rg{ring, full, empty, &s_abort};
-
-  if (tid == 0) {
-    for (int s = 0; s < C.nstages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+// The producer thread's drain after an abort: every copy it issued lands
+// before the CTA may move on or exit.
+__device__ __noinline__ void drain_ring(const Ring& rg, const KernelCfg& C, const RingPos& rp) {
+  const int it = rp.n;
+  for (int j = (it > C.nstages ? it - C.nstages : 0); j < it; ++j) {
+    const long long tw = clock64();
+    while (!mbar_try_wait(&rg.full[j % C.nstages], (j / C.nstages) & 1)) {
+      if (clock64() - tw > kWaitCycles) break;
     }
-    s_abort = 0;
+  }
+}
+
+// Shared-memory carve-up common to both kernels.
+struct Smem {
+  uint8_t* ring;
+  __half* bm;
+  __half* bs;
+  float4* red;
+  uint64_t* full;
+  uint64_t* empty;
+};
+__device__ __forceinline__ Smem carve(uint8_t* smem, const KernelCfg& C) {
+  Smem m;
+  m.ring = smem;
+  m.bm = reinterpret_cast<__half*>(smem + (size_t)C.nstages * C.stage_bytes);
+  m.bs = m.bm + (size_t)C.nsets * C.bmain_halves;
+  m.red = reinterpret_cast<float4*>(m.bs + (size_t)C.nsets * C.bsum_halves);
+  m.full = reinterpret_cast<uint64_t*>(m.red + 2 * kConsumerWarps * 32);
+  m.empty = m.full + kMaxStages;
+  return m;
+}
+
+__device__ __forceinline__ void init_cta(const KernelCfg& C, const Smem& m, volatile int* s_abort) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C.nstages; ++s) {
+      mbar_init(&m.full[s], 1);
+      mbar_init(&m.empty[s], kConsumerWarps);
+    }
+    *s_abort = 0;
     fence_mbar_init();
   }
   // padded block-sum slots are never written: zero the sums region once
-  for (int i = tid; i < C.nsets * C.bsum_halves / 2; i += blockDim.x) reinterpret_cast<uint32_t*>(bs)[i] = 0u;
-  for (int i = tid; i < 2 * kMaxExperts; i += blockDim.x) (&sp.wcnt[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < C.nsets * C.bsum_halves / 2; i += blockDim.x) reinterpret_cast<uint32_t*>(m.bs)[i] = 0u;
+}
 
-  // R: router partial logits, x fragments; then every CTA waits for all
-  router_stage<BITS>(L, W);
-  if (!grid_barrier(W, &sp.ok)) return;  // timed out: the error word says so
-
+// After stage R and its grid barrier: the routing plan, gate/up, down and the
+// combine of one MoE layer.  Returns false when the plan is unusable (the
+// error word says why); every CTA sees the same plan, so all return alike.
+template <int BITS>
+__device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, SPlan& sp,
+                                          const Ring& rg, const Smem& m, RingPos& rp, int& buf) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // P: the routing plan (the ring is free until the producer starts: logits scratch)
-  compute_plan(L, W, sp, reinterpret_cast<float*>(ring));
+  compute_plan(L, W, sp, reinterpret_cast<float*>(m.ring));
   const int nd = sp.nd;
   if (nd < 0 || nd > L.E) {
     if (tid == 0) atomicOr(W.err, kErrIndex);
-    return;
+    return false;
   }
   const bool has_shared = L.Fs > 0;
   if (warp == 0) {
@@ -1016,43 +1104,159 @@ __global__ void __launch_bounds__(kExpertThreads, 1) window_kernel(LayerDev L, W
   }
   __syncthreads();
 
-  RingPos rp;
+  const int ns0 = 2 * sp.pt[0].mt, ns1 = sp.pt[1].mt;
   if (warp == kConsumerWarps) {
     // ---------------- producer ----------------
     if (lane == 0) {
-      const int ns0 = 2 * sp.pt[0].mt, ns1 = sp.pt[1].mt;
       const bool ok = ns0 == 4 ? produce<BITS, 0, 4>(L, W, C, sp, rg, rp) : produce<BITS, 0, 2>(L, W, C, sp, rg, rp);
       if (ok) {
         if (ns1 == 4) produce<BITS, 1, 4>(L, W, C, sp, rg, rp);
         else if (ns1 == 2) produce<BITS, 1, 2>(L, W, C, sp, rg, rp);
         else produce<BITS, 1, 1>(L, W, C, sp, rg, rp);
       }
-      if (s_abort) {
-        // Let every copy this thread issued land before the CTA can exit.
-        const int it = rp.n;
-        for (int j = (it > C.nstages ? it - C.nstages : 0); j < it; ++j) {
-          const long long tw = clock64();
-          while (!mbar_try_wait(&full[j % C.nstages], (j / C.nstages) & 1)) {
-            if (clock64() - tw > kWaitCycles) break;
-          }
-        }
-      }
+      if (*rg.abort_flag) drain_ring(rg, C, rp);
+    }
+    return true;
+  }
+  if (ns0 == 4) consume<BITS, 0, 4>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+  else consume<BITS, 0, 2>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+  if (ns1 == 4) {
+    consume<BITS, 1, 4>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+    combine<4>(L, W, sp);
+  } else if (ns1 == 2) {
+    consume<BITS, 1, 2>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+    combine<2>(L, W, sp);
+  } else {
+    consume<BITS, 1, 1>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+    combine<1>(L, W, sp);
+  }
+  return true;
+}
+
+// One dense projection phase (2: [Wq; Wk; Wv] a, 3: x + Wo att) over all T
+// rows, its row tiles split evenly over the CTAs.
+template <int BITS, int PHASE>
+__device__ __forceinline__ void dense_phase(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, SPlan& sp,
+                                            const Ring& rg, const Smem& m, RingPos& rp, int& buf) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rows = PHASE == 2 ? L.dq + 2 * L.dkv : L.d;
+  if (tid == 0) {
+    PhaseTasks& p = sp.pt[PHASE];
+    const int tiles = rows / 16;
+    int mt = C.ph[PHASE].max_sub;
+    while (mt > 1 && (tiles % mt != 0 || tiles / mt < 2 * (int)gridDim.x)) mt >>= 1;
+    p.mt = mt;
+    p.ntask_s = tiles / mt;
+    p.ntask_e = 0;
+    p.t0 = (int)((long long)p.ntask_s * blockIdx.x / gridDim.x);
+    p.t1 = (int)((long long)p.ntask_s * (blockIdx.x + 1) / gridDim.x);
+  }
+  __syncthreads();
+  const int ns = sp.pt[PHASE].mt;
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      if (ns == 4) produce<BITS, PHASE, 4>(L, W, C, sp, rg, rp);
+      else if (ns == 2) produce<BITS, PHASE, 2>(L, W, C, sp, rg, rp);
+      else produce<BITS, PHASE, 1>(L, W, C, sp, rg, rp);
+      if (*rg.abort_flag) drain_ring(rg, C, rp);
     }
     return;
   }
-  const int ns0 = 2 * sp.pt[0].mt, ns1 = sp.pt[1].mt;
+  if (ns == 4) consume<BITS, PHASE, 4>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+  else if (ns == 2) consume<BITS, PHASE, 2>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+  else consume<BITS, PHASE, 1>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+}
+
+}  // namespace
+
+// Shared memory: [ring: nstages x stage_bytes][B main: nsets][B sums: nsets]
+// [red: 2 x 16 warps x 32 lanes float4][full/empty mbarriers]; static: SPlan.
+template <int BITS>
+__global__ void __launch_bounds__(kExpertThreads, 1) window_kernel(LayerDev L, WindowBufs W, KernelCfg C) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ volatile int s_abort;
+  __shared__ SPlan sp;
+  const Smem m = carve(smem, C);
+  const Ring rg{m.ring, m.full, m.empty, &s_abort};
+  init_cta(C, m, &s_abort);
+  for (int i = threadIdx.x; i < 2 * kMaxExperts; i += blockDim.x) (&sp.wcnt[0][0])[i] = 0;
+
+  // R: router partial logits, x fragments; then every CTA waits for all
+  router_stage<BITS>(L, W);
+  if (!grid_barrier(W, &sp.ok)) return;  // timed out: the error word says so
+  RingPos rp;
   int buf = 0;
-  if (ns0 == 4) consume<BITS, 0, 4>(L, W, C, sp, rg, bm, bs, red, rp, buf);
-  else consume<BITS, 0, 2>(L, W, C, sp, rg, bm, bs, red, rp, buf);
-  if (ns1 == 4) {
-    consume<BITS, 1, 4>(L, W, C, sp, rg, bm, bs, red, rp, buf);
-    combine<4>(L, W, sp);
-  } else if (ns1 == 2) {
-    consume<BITS, 1, 2>(L, W, C, sp, rg, bm, bs, red, rp, buf);
-    combine<2>(L, W, sp);
-  } else {
-    consume<BITS, 1, 1>(L, W, C, sp, rg, bm, bs, red, rp, buf);
-    combine<1>(L, W, sp);
+  moe_block<BITS>(L, W, C, sp, rg, m, rp, buf);
+}
+
+// A window through n decoder layers in one launch.  Per layer:
+//   D0. every CTA: 1/RMS of each row of x; all CTAs write the fragments of
+//       x / RMS(x);  grid barrier
+//   D1. [q; k; v] = [Wq; Wk; Wv] a;  grid barrier
+//   D2. x1 = x + Wo att, att = the grouped-query broadcast of v (a context of
+//       one position: every query head's softmax weight is 1);  grid barrier
+//   M.  the MoE window on x1 / RMS(x1) (stage R, grid barrier, plan, gate/up,
+//       down), its combine adding x1;  grid barrier
+// Layer l reads x from the previous layer's output (ping-pong buffers ybuf)
+// and the last layer writes y.
+template <int BITS>
+__global__ void __launch_bounds__(kExpertThreads, 1)
+    stack_kernel(const LayerDev* __restrict__ layers, int n_layers, WindowBufs Wp, KernelCfg C, const float* x_in,
+                 float* y_out, float* ybuf, float* q_all, float* k_all) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ volatile int s_abort;
+  __shared__ SPlan sp;
+  __shared__ LayerDev sL;
+  __shared__ WindowBufs sW;
+  __shared__ float s_rinv[kMaxRows];
+  const int tid = threadIdx.x;
+  const Smem m = carve(smem, C);
+  const Ring rg{m.ring, m.full, m.empty, &s_abort};
+  init_cta(C, m, &s_abort);
+  RingPos rp;
+  int buf = 0;
+  for (int l = 0; l < n_layers; ++l) {
+    if (tid == 0) {
+      sL = layers[l];
+      WindowBufs w = Wp;
+      const long long plane = (long long)kMaxRows * sL.d;
+      w.x = l == 0 ? x_in : ybuf + ((l - 1) & 1) * plane;
+      w.y = l == n_layers - 1 ? y_out : ybuf + (l & 1) * plane;
+      w.q_out = q_all ? q_all + (long long)l * Wp.T * sL.dq : nullptr;
+      w.k_out = k_all ? k_all + (long long)l * Wp.T * sL.dkv : nullptr;
+      w.rinv = s_rinv;
+      w.resid = nullptr;
+      const long long tk = (long long)l * Wp.T * sL.k;
+      w.out_topk_idx = Wp.out_topk_idx ? Wp.out_topk_idx + tk : nullptr;
+      w.out_topk_w = Wp.out_topk_w ? Wp.out_topk_w + tk : nullptr;
+      w.out_ndistinct = Wp.out_ndistinct ? Wp.out_ndistinct + l : nullptr;
+      w.out_counts = w.out_offsets = w.out_entries = w.out_distinct = nullptr;
+      sW = w;
+    }
+    for (int i = tid; i < 2 * kMaxExperts; i += blockDim.x) (&sp.wcnt[0][0])[i] = 0;
+    __syncthreads();
+    const LayerDev& L = sL;
+    // D0
+    row_rinv(sW.x, sW.T, L.d, s_rinv);
+    write_x_frags<BITS>(L, sW);
+    if (!grid_barrier(sW, &sp.ok)) return;
+    // D1
+    dense_phase<BITS, 2>(L, sW, C, sp, rg, m, rp, buf);
+    if (!grid_barrier(sW, &sp.ok) || s_abort) return;
+    // D2
+    dense_phase<BITS, 3>(L, sW, C, sp, rg, m, rp, buf);
+    if (!grid_barrier(sW, &sp.ok) || s_abort) return;
+    // M
+    if (tid == 0) {
+      sW.x = sW.x1;
+      sW.resid = sW.x1;
+    }
+    __syncthreads();
+    row_rinv(sW.x, sW.T, L.d, s_rinv);
+    router_stage<BITS>(L, sW);
+    if (!grid_barrier(sW, &sp.ok)) return;
+    if (!moe_block<BITS>(L, sW, C, sp, rg, m, rp, buf)) return;
+    if (!grid_barrier(sW, &sp.ok) || s_abort) return;
   }
 }
 
@@ -1114,8 +1318,12 @@ KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit) {
   KernelCfg C{};
   const int bits = L.bits;
   const int block = bits == 4 ? 32 : 16;
-  const int Kmax = L.d > (L.F > L.Fs ? L.F : L.Fs) ? L.d : (L.F > L.Fs ? L.F : L.Fs);
-  const int nmk = (Kmax / block + 15) / 16;
+  // B main holds the widest activation vector a phase stages (the dense o
+  // projection stages v and remaps k-steps); B sums cover the widest input
+  int Kmax = L.d > (L.F > L.Fs ? L.F : L.Fs) ? L.d : (L.F > L.Fs ? L.F : L.Fs);
+  if (L.dkv > Kmax) Kmax = L.dkv;
+  const int Ksum = L.dq > Kmax ? L.dq : Kmax;
+  const int nmk = (Ksum / block + 15) / 16;
   C.bmain_halves = 8 * Kmax;
   C.bsum_halves = nmk * 8 * 4 * 4;
   C.nsets = max_rows > 4 ? 2 : 1;
@@ -1126,6 +1334,13 @@ KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit) {
   C.ph[0] = phase_cfg(0, bits, L.d, L.d, budget, sb0);
   C.ph[1] = phase_cfg(1, bits, L.F, L.Fs > 0 ? L.Fs : L.F, budget, sb1);
   C.stage_bytes = sb0 > sb1 ? sb0 : sb1;
+  if (L.dq > 0) {  // decoder layer: the dense q/k/v and o phases
+    int sb2 = 0, sb3 = 0;
+    C.ph[2] = phase_cfg(1, bits, L.d, L.d, budget, sb2);
+    C.ph[3] = phase_cfg(1, bits, L.dq, L.dq, budget, sb3);
+    if (sb2 > C.stage_bytes) C.stage_bytes = sb2;
+    if (sb3 > C.stage_bytes) C.stage_bytes = sb3;
+  }
   int st = C.stage_bytes > 0 ? ring / C.stage_bytes : 0;
   C.nstages = st > kMaxStages ? kMaxStages : st;
   C.total_bytes = C.nstages * C.stage_bytes + fixed;
@@ -1162,6 +1377,40 @@ cudaError_t launch_window(const LayerDev& L, const WindowBufs& W, const KernelCf
   cfg.numAttrs = 1;
   if (L.bits == 4) return cudaLaunchKernelEx(&cfg, window_kernel<4>, L, W, C);
   return cudaLaunchKernelEx(&cfg, window_kernel<2>, L, W, C);
+}
+
+static const void* stack_fn(int bits) {
+  return bits == 4 ? (const void*)stack_kernel<4> : (const void*)stack_kernel<2>;
+}
+
+cudaError_t stack_set_attrs(int bits, int smem_bytes) {
+  return cudaFuncSetAttribute(stack_fn(bits), cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+}
+
+int stack_blocks_per_sm(int bits, int smem_bytes) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, stack_fn(bits), kExpertThreads, smem_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+cudaError_t launch_stack(const LayerDev* layers, int n_layers, int bits, const WindowBufs& W, const KernelCfg& C,
+                         int grid, const float* x, float* y, float* ybuf, float* q_all, float* k_all,
+                         cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kExpertThreads);
+  cfg.dynamicSmemBytes = C.total_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (bits == 4) return cudaLaunchKernelEx(&cfg, stack_kernel<4>, layers, n_layers, W, C, x, y, ybuf, q_all, k_all);
+  return cudaLaunchKernelEx(&cfg, stack_kernel<2>, layers, n_layers, W, C, x, y, ybuf, q_all, k_all);
 }
 
 }  // namespace strata

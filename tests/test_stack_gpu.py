@@ -1,0 +1,142 @@
+"""GPU parity of the decoder-layer stack (RMSNorm, dense q/k/v/o, length-1
+attention, MoE with residuals) against the fp64 oracle, through the C ABI.
+
+Routing must match the oracle bit for bit at every layer; rows are drawn so
+that the fp64 top-k margin is >= 1e-3 at every layer.  y, q and k must
+satisfy max|err| <= 2e-3 * RMS(oracle) over the compared rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+from slot_decode_window_gb300 import workloads as wlm
+from tests.helpers import MARGIN, odense, omoe, omoe_lazy, stack_trajectory
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from slot_decode_window_gb300 import binding, build
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    build.build()
+    binding.load()
+
+
+def _layers(wl, n, seed=0):
+    moe = [wlm.make_moe_layer(wl.moe, seed=seed, cfg_id=wl.cfg_id, layer=l, device="cuda") for l in range(n)]
+    dense = [wlm.make_dense_layer(wl, seed=seed, layer=l, device="cuda") for l in range(n)]
+    return moe, dense
+
+
+class _Traj:
+    """Memoised oracle trajectories; accepts rows whose margin holds at every layer."""
+
+    def __init__(self, dense_o, moe_o):
+        self.dense_o, self.moe_o, self.memo = dense_o, moe_o, {}
+
+    def __call__(self, row):
+        return self.get(row)[4] >= MARGIN
+
+    def get(self, row):
+        key = row.tobytes()
+        if key not in self.memo:
+            self.memo[key] = stack_trajectory(row, self.dense_o, self.moe_o)
+        return self.memo[key]
+
+
+def _compare(res, y, x, traj, rows, n_layers):
+    """Routing exact at every layer; y, q, k within tolerance on the given rows."""
+    got_idx = res["topk_idx"].cpu().numpy()
+    qg, kg = res["q"].cpu().numpy().astype(np.float64), res["k"].cpu().numpy().astype(np.float64)
+    ref_y, ref_q, ref_k = [], [], []
+    for t in rows:
+        yo, qs, ks, sels, margin = traj.get(x[t])
+        assert margin >= MARGIN
+        for l in range(n_layers):
+            np.testing.assert_array_equal(got_idx[l, t], sels[l], err_msg=f"layer {l} row {t}")
+        ref_y.append(yo)
+        ref_q.append(np.stack(qs))
+        ref_k.append(np.stack(ks))
+    ref_y = np.stack(ref_y)
+    yg = y[rows]
+    assert np.isfinite(yg).all()
+    rms = np.sqrt(np.mean(ref_y * ref_y))
+    err = np.abs(yg - ref_y).max()
+    assert err <= TOL * rms, f"y: max err {err:.3e} > {TOL} * rms {rms:.3e}"
+    for name, g, r in (("q", qg, ref_q), ("k", kg, ref_k)):
+        r = np.stack(r)                      # [rows][L][w]
+        gs = np.transpose(g[:, rows], (1, 0, 2))
+        for l in range(n_layers):
+            rl = r[:, l]
+            e = np.abs(gs[:, l] - rl).max()
+            assert e <= TOL * np.sqrt(np.mean(rl * rl)), f"{name} layer {l}: max err {e:.3e}"
+
+
+SMALL = [
+    wlm.Workload("stack_small_a", 91, wlm.MoESpec(256, 8, 2, 128, 128, 4, 32), (1,), n_layers=3,
+                 heads=4, kv_heads=2, head_dim=64),
+    wlm.Workload("stack_small_b", 92, wlm.MoESpec(256, 12, 3, 192, 64, 4, 32), (1,), n_layers=2,
+                 heads=8, kv_heads=2, head_dim=128),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("T", [1, 5, 8])
+def test_small_stack_all_rows(wl, T):
+    from slot_decode_window_gb300.binding import Stack
+    moe, dense = _layers(wl, wl.n_layers)
+    traj = _Traj([odense(dl, wl) for dl in dense], [omoe(m) for m in moe])
+    x = wlm.make_window(wl, T, seed=0, window=T, accept_row=traj)
+    stk = Stack(wl, moe, dense, max_rows=8)
+    y, res = stk.forward(torch.from_numpy(x).cuda(), outputs=True)
+    stk.sync()
+    _compare(res, y.cpu().numpy().astype(np.float64), x, traj, list(range(T)), wl.n_layers)
+    stk.close()
+
+
+def test_stack48_shapes_three_layers_all_rows():
+    """The 48-layer stack's per-layer shapes (d 2048, 32/4 heads of 128, 128 experts top-8), three layers."""
+    from slot_decode_window_gb300.binding import Stack
+    base = wlm.WORKLOADS["stack48"]
+    wl = wlm.Workload("stack48", base.cfg_id, base.moe, (8,), n_layers=3)
+    moe, dense = _layers(wl, 3)
+    traj = _Traj([odense(dl, wl) for dl in dense], [omoe_lazy(m) for m in moe])
+    x = wlm.make_window(wl, 8, seed=0, window=0, accept_row=traj)
+    stk = Stack(wl, moe, dense, max_rows=8)
+    y, res = stk.forward(torch.from_numpy(x).cuda(), outputs=True)
+    stk.sync()
+    _compare(res, y.cpu().numpy().astype(np.float64), x, traj, list(range(8)), 3)
+    stk.close()
+
+
+def test_stack48_full_depth_sampled_row_and_determinism():
+    """All 48 layers, T = 8 (the full workload): one sampled row whose fp64 margin
+    holds at every layer is checked against the oracle; the run repeats bit for bit."""
+    from slot_decode_window_gb300.binding import Stack
+    wl = wlm.WORKLOADS["stack48"]
+    moe, dense = _layers(wl, wl.n_layers)
+    stk = Stack(wl, moe, dense, max_rows=8)
+    x = wlm.make_window(wl, 8, seed=0, window=0)
+    xt = torch.from_numpy(x).cuda()
+    y1, res = stk.forward(xt, outputs=True)
+    y2 = stk.forward(xt)
+    stk.sync()
+    y1n, y2n = y1.cpu().numpy(), y2.cpu().numpy()
+    np.testing.assert_array_equal(y1n, y2n)
+    assert np.isfinite(y1n).all()
+    idx = res["topk_idx"].cpu().numpy()
+    assert idx.min() >= 0 and idx.max() < wl.moe.n_experts
+    nd = res["n_distinct"].cpu().numpy()
+    assert (nd >= wl.moe.top_k).all() and (nd <= 8 * wl.moe.top_k).all()
+    traj = _Traj([odense(dl, wl) for dl in dense], [omoe_lazy(m) for m in moe])
+    checked = 0
+    for t in range(3):
+        if traj(x[t]):
+            _compare(res, y1n.astype(np.float64), x, traj, [t], wl.n_layers)
+            checked += 1
+            break
+    assert checked == 1, "no sampled row kept a 1e-3 margin at every layer"
+    stk.close()
