@@ -51,7 +51,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-stack", action="store_true", help="skip the 48-layer stack measurement")
     p.add_argument("--stack-steps", type=int, default=30)
-    p.add_argument("--mode", choices=("full", "windows"), default="full",
+    p.add_argument("--stack-layers", type=int, default=2, help="layers of the stack in --mode stack")
+    p.add_argument("--mode", choices=("full", "windows", "stack"), default="full",
                    help="windows: only warmup + K windows at --rows (a clean launch sequence for ncu)")
     return p.parse_args()
 
@@ -260,6 +261,26 @@ def run_ours(args, rank, world, local_rank):
     win = binding.Window(layer, max_rows=8)
     info = win.info()
     stream = torch.cuda.current_stream()
+
+    if args.mode == "stack":
+        # a short run of the decoder-layer stack kernel (for profilers): the
+        # 48-layer stack's per-layer shapes, --stack-layers layers, T = --rows
+        wls = wlm.WORKLOADS["stack48"]
+        n = args.stack_layers
+        moe = [wlm.make_moe_layer(wls.moe, seed=0, cfg_id=wls.cfg_id, layer=l, device=str(dev)) for l in range(n)]
+        dense = [wlm.make_dense_layer(wls, seed=0, layer=l, device=str(dev)) for l in range(n)]
+        stk = binding.Stack(wls, moe, dense, max_rows=8)
+        T = args.rows
+        xw = torch.from_numpy(np.stack([wlm.make_window(wls, T, seed=0, window=w) for w in range(4)])).to(dev)
+        yw = torch.empty(T, wls.moe.hidden, device=dev)
+        for i in range(args.warmup + args.steps):
+            stk.forward(xw[i % 4], yw)
+        stk.sync()
+        if rank == 0:
+            print(json.dumps({"mode": "stack", "layers": n, "T": T, "windows": args.steps}), flush=True)
+        stk.close()
+        win.close()
+        return
 
     if args.mode == "windows":
         T = args.rows
