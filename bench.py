@@ -364,6 +364,26 @@ def run_ours(args, rank, world, local_rank):
                            "algorithmic_GBps": b / tot / 1e9,
                            "mean_distinct_experts": sum(nd[Ts_]) / len(nd[Ts_])}
 
+    # the same windows through the handle's CUDA-graph cache (fixed x/y buffers)
+    xg = torch.empty(T, d, device=dev)
+    yg = torch.empty(T, d, device=dev)
+    for i in range(3):
+        xg.copy_(X[T][i])
+        win.forward_graph(xg, yg)
+    g_ms = []
+    for i in range(min(args.steps, 500)):
+        xg.copy_(X[T][i % N_WINDOWS])
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        win.forward_graph(xg, yg)
+        b.record(stream)
+        g_ms.append((a, b))
+    torch.cuda.synchronize()
+    g_ms = [a.elapsed_time(b) for a, b in g_ms]
+    graph = {"T": T, "windows": len(g_ms), "us_per_window_median": 1e3 * statistics.median(g_ms),
+             "rows_per_s": len(g_ms) * T / (sum(g_ms) / 1e3), "path": "strata_moe_window_forward_graph"}
+
     # window kernel roofline: events right around the kernel (profiling mode)
     win.set_profiling(True)
     prof_steps = min(args.steps, 400)
@@ -432,7 +452,7 @@ def run_ours(args, rank, world, local_rank):
                        "parallelism": "replicas only" if world > 1 else "1 GPU",
                        "arith": "codes -> exact fp16 integers; mma.sync f16 x (fp16 hi + lo activations), fp32 "
                                 "accumulate; fp32 router, softmax, SwiGLU, combine"},
-            "roofline": roofline, "sweep": sweep, "stack48": stack, "e2e": e2e, "clocks": clocks,
+            "roofline": roofline, "sweep": sweep, "graph": graph, "stack48": stack, "e2e": e2e, "clocks": clocks,
             "cpu_baseline": cpu,
             "gpu_launches": args.steps,
             "window_us_median": 1e3 * statistics.median(ms), "wall_s_timed_region": wall,

@@ -133,6 +133,18 @@ strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe
 strata_status strata_moe_window_forward(strata_window* h, const float* x, int32_t T, float* y,
                                         const strata_routing_out* routing, void* cuda_stream);
 
+/* Run one window like strata_moe_window_forward (no routing outputs) by
+ * replaying a CUDA graph of the window launch.  The handle keeps a bounded
+ * cache of 16 instantiated graphs keyed by (T, x, y): the first call with a
+ * key captures and instantiates its graph (on a stream the handle owns),
+ * later calls only launch it; the least recently used graph is evicted when
+ * the cache is full.  The Strata pages' pull request on windows with MTP rows
+ * describes eight-row windows run through a bounded batch graph cache; this
+ * is that cache for the one-launch window.  Returns EINVAL as the plain
+ * forward, ECUDA if capture, instantiation or launch fails. */
+strata_status strata_moe_window_forward_graph(strata_window* h, const float* x, int32_t T, float* y,
+                                              void* cuda_stream);
+
 /* Wait for the handle's last forward call to finish; report (and clear) any
  * error the GPU recorded: EDEVICE in that case. */
 strata_status strata_window_sync(strata_window* h);

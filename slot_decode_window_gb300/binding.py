@@ -22,7 +22,7 @@ STRATA_OK, STRATA_EINVAL, STRATA_ENOMEM, STRATA_ECUDA, STRATA_EUNSUPPORTED, STRA
 
 EXPORTED = ("strata_window_create", "strata_moe_window_forward", "strata_window_sync", "strata_window_query",
             "strata_window_set_profiling", "strata_window_timings", "strata_window_destroy", "strata_status_str",
-            "strata_moe_window_forward_noalloc", "strata_stack_create", "strata_stack_forward", "strata_stack_sync",
+            "strata_moe_window_forward_noalloc", "strata_moe_window_forward_graph", "strata_stack_create", "strata_stack_forward", "strata_stack_sync",
             "strata_stack_query", "strata_stack_set_profiling", "strata_stack_timings", "strata_stack_destroy")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -97,6 +97,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.strata_moe_window_forward.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                               P(strata_routing_out), ctypes.c_void_p]
     lib.strata_moe_window_forward.restype = ctypes.c_int
+    lib.strata_moe_window_forward_graph.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                                    ctypes.c_void_p, ctypes.c_void_p]
+    lib.strata_moe_window_forward_graph.restype = ctypes.c_int
     lib.strata_moe_window_forward_noalloc.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                                       ctypes.c_void_p, ctypes.c_void_p]
     lib.strata_moe_window_forward_noalloc.restype = ctypes.c_int
@@ -154,6 +157,11 @@ def strata_moe_window_forward(handle, x_ptr: int, T: int, y_ptr: int, routing: O
                                             ctypes.c_void_p(y_ptr),
                                             ctypes.byref(routing) if routing is not None else None,
                                             ctypes.c_void_p(stream))
+
+
+def strata_moe_window_forward_graph(handle, x_ptr: int, T: int, y_ptr: int, stream: int = 0) -> int:
+    return load().strata_moe_window_forward_graph(ctypes.c_void_p(handle), ctypes.c_void_p(x_ptr), T,
+                                                  ctypes.c_void_p(y_ptr), ctypes.c_void_p(stream))
 
 
 def strata_moe_window_forward_noalloc(handle, x_ptr: int, T: int, y_ptr: int, stream: int = 0) -> int:
@@ -295,6 +303,15 @@ class Window:
         check(strata_moe_window_forward(self.handle, x.data_ptr(), T, y.data_ptr(), r, s),
               "strata_moe_window_forward")
         return (y, rt) if routing else y
+
+    def forward_graph(self, x, y, stream=None):
+        """Enqueue one window through the handle's graph cache (x, y fixed CUDA buffers)."""
+        import torch
+        assert x.is_cuda and x.dtype == torch.float32 and x.is_contiguous() and y.is_contiguous()
+        s = (stream or torch.cuda.current_stream()).cuda_stream
+        check(strata_moe_window_forward_graph(self.handle, x.data_ptr(), x.shape[0], y.data_ptr(), s),
+              "strata_moe_window_forward_graph")
+        return y
 
     def set_profiling(self, enable: bool) -> None:
         check(strata_window_set_profiling(self.handle, enable), "strata_window_set_profiling")

@@ -3,6 +3,16 @@
 #include "common.cuh"
 #include "strata_window.h"
 
+// One instantiated CUDA graph of a window launch, keyed by its arguments.
+struct strata_graph_entry {
+  int T = 0;
+  const float* x = nullptr;
+  float* y = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  unsigned long long last_use = 0;
+};
+constexpr int kGraphCache = 16;  // graphs a handle keeps (least recently used evicted)
+
 struct strata_window {
   strata_moe_desc desc;
   int device = 0;
@@ -18,6 +28,9 @@ struct strata_window {
   bool profiling = false;
   bool profiled_once = false;
   cudaEvent_t prof[2] = {nullptr, nullptr};
+  strata_graph_entry graphs[kGraphCache];
+  unsigned long long graph_clock = 0;
+  cudaStream_t capture_stream = nullptr;
 };
 
 namespace strata {

@@ -56,6 +56,9 @@ long long qmat_bytes(int n, int rows, int cols, int bits, int block) {
 
 void free_handle(strata_window* h) {
   if (!h) return;
+  for (strata_graph_entry& g : h->graphs)
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+  if (h->capture_stream) cudaStreamDestroy(h->capture_stream);
   if (h->done) cudaEventDestroy(h->done);
   for (cudaEvent_t& ev : h->prof)
     if (ev) cudaEventDestroy(ev);
@@ -253,6 +256,74 @@ strata_status strata_moe_window_forward(strata_window* h, const float* x, int32_
   if (e == cudaSuccess && prof) e = cudaEventRecord(h->prof[1], s);
   if (e == cudaSuccess) e = cudaEventRecord(h->done, s);
   if (e == cudaSuccess && prof) h->profiled_once = true;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return STRATA_ECUDA;
+  }
+  return STRATA_OK;
+}
+
+strata_status strata_moe_window_forward_graph(strata_window* h, const float* x, int32_t T, float* y,
+                                              void* cuda_stream) {
+  if (!h || !x || !y) return STRATA_EINVAL;
+  if (T < 1 || T > h->desc.max_rows) return STRATA_EINVAL;
+  const size_t bytes = (size_t)T * h->desc.hidden * sizeof(float);
+  const char* xb = reinterpret_cast<const char*>(x);
+  const char* yb = reinterpret_cast<const char*>(y);
+  if (xb < yb + bytes && yb < xb + bytes) return STRATA_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) % 16 != 0) return STRATA_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+
+  strata_graph_entry* hit = nullptr;
+  strata_graph_entry* victim = &h->graphs[0];
+  for (strata_graph_entry& g : h->graphs) {
+    if (g.exec && g.T == T && g.x == x && g.y == y) {
+      hit = &g;
+      break;
+    }
+    if (!g.exec || (victim->exec && g.last_use < victim->last_use)) victim = &g;
+  }
+  if (!hit) {
+    // capture the window launch on the handle's own stream and instantiate it
+    if (!h->capture_stream && cudaStreamCreateWithFlags(&h->capture_stream, cudaStreamNonBlocking) != cudaSuccess) {
+      cudaGetLastError();
+      return STRATA_ECUDA;
+    }
+    WindowBufs W = h->W;
+    W.x = x;
+    W.y = y;
+    W.T = T;
+    W.out_topk_idx = nullptr;
+    W.out_topk_w = nullptr;
+    W.out_counts = nullptr;
+    W.out_offsets = nullptr;
+    W.out_entries = nullptr;
+    W.out_distinct = nullptr;
+    W.out_ndistinct = nullptr;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(h->capture_stream, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+      const cudaError_t el = launch_window(h->L, W, h->cfg, h->nsm, h->capture_stream);
+      e = cudaStreamEndCapture(h->capture_stream, &graph);
+      if (el != cudaSuccess) e = el;
+    }
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&exec, graph, 0);
+    if (graph) cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return STRATA_ECUDA;
+    }
+    if (victim->exec) cudaGraphExecDestroy(victim->exec);
+    victim->T = T;
+    victim->x = x;
+    victim->y = y;
+    victim->exec = exec;
+    hit = victim;
+  }
+  hit->last_use = ++h->graph_clock;
+  cudaError_t e = cudaGraphLaunch(hit->exec, s);
+  if (e == cudaSuccess) e = cudaEventRecord(h->done, s);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return STRATA_ECUDA;
