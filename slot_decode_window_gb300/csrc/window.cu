@@ -89,17 +89,16 @@ __device__ __forceinline__ int bmain_off(int ks, int p, int col, int c) {
 // bk points at this lane's slot of plane 0 of the k-step (set 0).
 template <int BITS, bool PAIRED>
 __device__ __forceinline__ void kstep_mma(const uint8_t* __restrict__ ch, const __half* __restrict__ bk, int bm_set,
-                                          bool bon, int lane, float (&acc)[4]) {
+                                          int lane, float (&acc)[4]) {
   const int g = lane >> 2;
   const float z4[4] = {0.f, 0.f, 0.f, 0.f};
-  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   if constexpr (BITS == 4) {
-    const uint4 bA = bon ? *reinterpret_cast<const uint4*>(bk) : z;
-    const uint4 bB = bon ? *reinterpret_cast<const uint4*>(bk + 256) : z;
+    const uint4 bA = *reinterpret_cast<const uint4*>(bk);
+    const uint4 bB = *reinterpret_cast<const uint4*>(bk + 256);
     uint4 lA = bA, lB = bB;
     if constexpr (!PAIRED) {
-      lA = bon ? *reinterpret_cast<const uint4*>(bk + bm_set) : z;
-      lB = bon ? *reinterpret_cast<const uint4*>(bk + bm_set + 256) : z;
+      lA = *reinterpret_cast<const uint4*>(bk + bm_set);
+      lB = *reinterpret_cast<const uint4*>(bk + bm_set + 256);
     }
     const uint4 cw = *reinterpret_cast<const uint4*>(ch + lane * 16);
     const uint2 sr = *reinterpret_cast<const uint2*>(ch + 512 + g * 8);
@@ -137,9 +136,9 @@ __device__ __forceinline__ void kstep_mma(const uint8_t* __restrict__ ch, const 
     const uint32_t sbv[4] = {sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint4 b = bon ? *reinterpret_cast<const uint4*>(bk + 256 * j) : z;
+      const uint4 b = *reinterpret_cast<const uint4*>(bk + 256 * j);
       uint4 l = b;
-      if constexpr (!PAIRED) l = bon ? *reinterpret_cast<const uint4*>(bk + bm_set + 256 * j) : z;
+      if constexpr (!PAIRED) l = *reinterpret_cast<const uint4*>(bk + bm_set + 256 * j);
       const uint32_t w = cwv[j], w2 = w >> 8;
       const float2 sgp = __half22float2(*reinterpret_cast<const __half2*>(&sav[j]));
       const float2 s8p = __half22float2(*reinterpret_cast<const __half2*>(&sbv[j]));
@@ -175,30 +174,29 @@ __device__ __forceinline__ void kstep_mma(const uint8_t* __restrict__ ch, const 
 template <int BITS, bool PAIRED, bool VMAP = false>
 __device__ __forceinline__ void chunk_mma(const uint8_t* __restrict__ sub, int mins_off, int ks_base, int k0, int k1,
                                           int mk_base, int m0, int m1, const __half* __restrict__ bm,
-                                          const __half* __restrict__ bs, int bm_set, int bs_set, bool bon, int lane,
+                                          const __half* __restrict__ bs, int bm_set, int bs_set, int lane_b, int lane,
                                           float (&acc)[4], float (&accm)[4], int kph = 0, int kpg = 0) {
   constexpr int S = Fmt<BITS>::kBHalves;
   const uint8_t* a = sub + k0 * Fmt<BITS>::kChunk;
-  const __half* bk = bm + (ks_base + k0) * 32 * S + lane * 8;
+  const __half* bk = bm + (ks_base + k0) * 32 * S + lane_b * 8;
 #pragma unroll 2
   for (int kl = k0; kl < k1; ++kl) {
     if constexpr (VMAP) {
       const int ks = ks_base + kl;
-      bk = bm + (((ks >> kpg) << kph) + (ks & ((1 << kph) - 1))) * 32 * S + lane * 8;
+      bk = bm + (((ks >> kpg) << kph) + (ks & ((1 << kph) - 1))) * 32 * S + lane_b * 8;
     }
-    kstep_mma<BITS, PAIRED>(a, bk, bm_set, bon, lane, acc);
+    kstep_mma<BITS, PAIRED>(a, bk, bm_set, lane, acc);
     a += Fmt<BITS>::kChunk;
     bk += 32 * S;
   }
   const uint8_t* am_p = sub + mins_off + m0 * 512 + lane * 16;
-  const __half* sp = bs + (mk_base + m0) * 128 + lane * 4;
-  const uint2 z = make_uint2(0u, 0u);
+  const __half* sp = bs + (mk_base + m0) * 128 + lane_b * 4;
   for (int ml = m0; ml < m1; ++ml) {
-    const uint2 b = bon ? *reinterpret_cast<const uint2*>(sp) : z;
+    const uint2 b = *reinterpret_cast<const uint2*>(sp);
     const uint4 am = *reinterpret_cast<const uint4*>(am_p);
     mma16816(accm, am.x, am.y, am.z, am.w, b.x, b.y, accm);
     if constexpr (!PAIRED) {
-      const uint2 l = bon ? *reinterpret_cast<const uint2*>(sp + bs_set) : z;
+      const uint2 l = *reinterpret_cast<const uint2*>(sp + bs_set);
       mma16816(accm, am.x, am.y, am.z, am.w, l.x, l.y, accm);
     }
     am_p += 512;
@@ -829,6 +827,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
   int cur = -2;
   int R = 0, ent_off = 0;
   bool paired = true, bon = true;
+  int lane_b = lane;
   uint32_t inv_d = 0;  // ceil(2^16 / (16 R)): i / (16 R) == (i * inv_d) >> 16 for i < 512
   TaskWalk tw;
   if (pt.t0 < pt.t1) tw.start(pt.t0, pt, has_shared, sp);
@@ -850,6 +849,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
       }
       paired = R <= 4;
       bon = paired ? (g < 2 * R) : (g < R);
+      lane_b = bon ? lane : (lane & 3);
       inv_d = (65536u + 16u * R - 1u) / (16u * R);
       if (PHASE == 1) {
         // wait (bounded) until every gate/up task of this group has landed
@@ -886,10 +886,10 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
         constexpr bool kVmap = PHASE == 3;
         if (paired)
           chunk_mma<BITS, true, kVmap>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
-                                       C.bsum_halves, bon, lane, acc, accm, L.kph_log2, L.kpg_log2);
+                                       C.bsum_halves, lane_b, lane, acc, accm, L.kph_log2, L.kpg_log2);
         else
           chunk_mma<BITS, false, kVmap>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
-                                        C.bsum_halves, bon, lane, acc, accm, L.kph_log2, L.kpg_log2);
+                                        C.bsum_halves, lane_b, lane, acc, accm, L.kph_log2, L.kpg_log2);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&rg.empty[stage]);
@@ -901,7 +901,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
     consumer_sync();
 
     // ---------------- epilogue: cross-warp sums in a fixed order ----------------
-    const int eo = (tid & 31) * kConsumerWarps + (tid >> 5);  // this thread's first output
+    const int eo = (tid + 32 * (task & (kConsumerWarps - 1))) & (kConsumerThreads - 1);
     if (PHASE == 0) {
       for (int i = eo; i < kMT * 16 * R; i += kConsumerThreads) {
         const int m = (int)(((uint32_t)i * inv_d) >> 16), rem = i - m * 16 * R;
@@ -1021,6 +1021,44 @@ __device__ void combine(const LayerDev& L, const WindowBufs& W, SPlan& sp) {
   for (int i = tid; i < nf * W.T * 4; i += kConsumerThreads) sum_quad(sp.finish[i / (W.T * 4)], i % (W.T * 4));
 }
 
+// The combine for windows of kGridCombineRows rows or more, after a grid
+// barrier that follows every CTA's down tasks: y = s + x1 + sum_j o[t k + j]
+// (shared expert first, the residual if any, then the k weighted expert
+// outputs in entry order), four outputs per thread, each CTA a contiguous
+// range, every load issued before the sums.  Smaller windows keep the
+// per-slice combine above: with few rows its tail is shorter than a barrier.
+constexpr int kGridCombineRows = 4;
+
+__device__ __noinline__ void combine_all(const LayerDev& L, const WindowBufs& W) {
+  const int nq = W.T * (L.d / 4);
+  const int q0 = (int)((long long)nq * blockIdx.x / gridDim.x), q1 = (int)((long long)nq * (blockIdx.x + 1) / gridDim.x);
+  const bool has_shared = L.Fs > 0;
+  for (int q = q0 + (int)threadIdx.x; q < q1; q += blockDim.x) {
+    const int t = q / (L.d / 4), rr = (q - t * (L.d / 4)) * 4;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 y = has_shared ? __ldcg(reinterpret_cast<const float4*>(W.sbuf + (long long)t * L.d + rr)) : z;
+    const float4 x1 = W.resid ? __ldcg(reinterpret_cast<const float4*>(W.resid + (long long)t * L.d + rr)) : z;
+    float4 o[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      o[j] = j < L.k ? __ldcg(reinterpret_cast<const float4*>(W.obuf + (long long)(t * L.k + j) * L.d + rr)) : z;
+    y.x += x1.x;
+    y.y += x1.y;
+    y.z += x1.z;
+    y.w += x1.w;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < L.k) {
+        y.x += o[j].x;
+        y.y += o[j].y;
+        y.z += o[j].z;
+        y.w += o[j].w;
+      }
+    }
+    *reinterpret_cast<float4*>(W.y + (long long)t * L.d + rr) = y;
+  }
+}
+
 // The producer thread's drain after an abort: every copy it issued lands
 // before the CTA may move on or exit.
 __device__ __noinline__ void drain_ring(const Ring& rg, const KernelCfg& C, const RingPos& rp) {
@@ -1066,9 +1104,11 @@ __device__ __forceinline__ void init_cta(const KernelCfg& C, const Smem& m, vola
   for (int i = threadIdx.x; i < C.nsets * C.bsum_halves / 2; i += blockDim.x) reinterpret_cast<uint32_t*>(m.bs)[i] = 0u;
 }
 
-// After stage R and its grid barrier: the routing plan, gate/up, down and the
-// combine of one MoE layer.  Returns false when the plan is unusable (the
-// error word says why); every CTA sees the same plan, so all return alike.
+// After stage R and its grid barrier: the routing plan, gate/up and down of one
+// MoE layer, and for windows of fewer than kGridCombineRows rows the per-slice
+// combine (larger windows combine after a grid barrier, in the caller).
+// Returns false when the plan is unusable (the error word says why); every
+// CTA sees the same plan, so all return alike.
 template <int BITS>
 __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, SPlan& sp,
                                           const Ring& rg, const Smem& m, RingPos& rp, int& buf) {
@@ -1120,15 +1160,16 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
   }
   if (ns0 == 4) consume<BITS, 0, 4>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
   else consume<BITS, 0, 2>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+  const bool slices = W.T < kGridCombineRows;  // else the caller combines after a grid barrier
   if (ns1 == 4) {
     consume<BITS, 1, 4>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
-    combine<4>(L, W, sp);
+    if (slices) combine<4>(L, W, sp);
   } else if (ns1 == 2) {
     consume<BITS, 1, 2>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
-    combine<2>(L, W, sp);
+    if (slices) combine<2>(L, W, sp);
   } else {
     consume<BITS, 1, 1>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
-    combine<1>(L, W, sp);
+    if (slices) combine<1>(L, W, sp);
   }
   return true;
 }
@@ -1186,7 +1227,11 @@ __global__ void __launch_bounds__(kExpertThreads, 1) window_kernel(LayerDev L, W
   if (!grid_barrier(W, &sp.ok)) return;  // timed out: the error word says so
   RingPos rp;
   int buf = 0;
-  moe_block<BITS>(L, W, C, sp, rg, m, rp, buf);
+  if (!moe_block<BITS>(L, W, C, sp, rg, m, rp, buf)) return;
+  if (W.T >= kGridCombineRows) {
+    if (!grid_barrier(W, &sp.ok) || s_abort) return;
+    combine_all(L, W);
+  }
 }
 
 // A window through n decoder layers in one launch.  Per layer:
@@ -1256,6 +1301,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1)
     router_stage<BITS>(L, sW);
     if (!grid_barrier(sW, &sp.ok)) return;
     if (!moe_block<BITS>(L, sW, C, sp, rg, m, rp, buf)) return;
+    if (sW.T >= kGridCombineRows) {
+      if (!grid_barrier(sW, &sp.ok) || s_abort) return;
+      combine_all(L, sW);
+    }
     if (!grid_barrier(sW, &sp.ok) || s_abort) return;
   }
 }
