@@ -86,7 +86,9 @@ __device__ __forceinline__ int bmain_off(int ks, int p, int col, int c) {
 }
 
 // One k-step of one sub-tile.  acc is in units of 2^-24 (subnormal codes).
-// bk points at this lane's slot of plane 0 of the k-step (set 0).
+// bk points at this lane's slot of plane 0 of the k-step (set 0); lanes whose
+// MMA column is unused point at column 0 instead (same-address reads
+// broadcast, and a column of the product depends only on that column of B).
 template <int BITS, bool PAIRED>
 __device__ __forceinline__ void kstep_mma(const uint8_t* __restrict__ ch, const __half* __restrict__ bk, int bm_set,
                                           int lane, float (&acc)[4]) {
@@ -901,6 +903,8 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
     consumer_sync();
 
     // ---------------- epilogue: cross-warp sums in a fixed order ----------------
+    // outputs on consecutive threads of one or two warps, rotating with the task,
+    // so the other warps go straight on to the next task
     const int eo = (tid + 32 * (task & (kConsumerWarps - 1))) & (kConsumerThreads - 1);
     if (PHASE == 0) {
       for (int i = eo; i < kMT * 16 * R; i += kConsumerThreads) {
