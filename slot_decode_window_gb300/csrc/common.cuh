@@ -97,8 +97,14 @@ struct WindowBufs {
   int* out_entries; int* out_distinct; int* out_ndistinct;
   // workspace
   __half* xfrag;           // [kMaxRows][frag(d)]
-  float2* gu;              // [kMaxEntries][F]: (Wg h, Wu h) of each routed entry
-  float2* sgu;             // [kMaxRows][Fs]: the same for the shared expert
+  // h = silu(Wg x) * (Wu x) of each routed entry, written by the gate/up
+  // epilogue already in activation-fragment form: fp16 hi then lo parts of
+  // F elements each (the x-fragment main layout), plus fp32 sums of h over
+  // every 16 consecutive elements (block sums are 1 or 2 of these)
+  __half* hfrag;           // [kMaxEntries][2F]
+  float* hsum;             // [kMaxEntries][F/16]
+  __half* shfrag;          // [kMaxRows][2Fs] the same for the shared expert
+  float* shsum;            // [kMaxRows][Fs/16]
   float* obuf;             // [kMaxEntries][d]
   float* sbuf;             // [kMaxRows][d]
   int* counters;           // [d/16] contributions landed per 16-row slice of y
@@ -146,6 +152,13 @@ struct KernelCfg {
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+
+// 16-byte asynchronous copy global -> shared (L2 only), and the wait for all
+// of this thread's outstanding ones.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }

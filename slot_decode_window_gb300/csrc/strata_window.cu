@@ -140,8 +140,10 @@ strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe
   const size_t o_done = w; w = align_up(w + (size_t)(E + 1) * 4, 256);
   const size_t o_part = w; w = align_up(w + (size_t)njb * kMaxRows * E * 4, 256);
   const size_t o_xf = w; w = align_up(w + (size_t)kMaxRows * frag_halves(d, nmk_d) * 2, 256);
-  const size_t o_gu = w; w = align_up(w + (size_t)kMaxEntries * F * 8, 256);
-  const size_t o_sgu = w; w = align_up(w + (size_t)kMaxRows * Fs * 8, 256);
+  const size_t o_hf = w; w = align_up(w + (size_t)kMaxEntries * 2 * F * 2, 256);
+  const size_t o_hs = w; w = align_up(w + (size_t)kMaxEntries * (F / 16) * 4, 256);
+  const size_t o_shf = w; w = align_up(w + (size_t)kMaxRows * 2 * Fs * 2, 256);
+  const size_t o_shs = w; w = align_up(w + (size_t)kMaxRows * (Fs / 16) * 4, 256);
   const size_t o_ob = w; w = align_up(w + (size_t)kMaxEntries * d * 4, 256);
   const size_t o_sb = w; w = align_up(w + (size_t)kMaxRows * d * 4, 256);
   h->ws_bytes = (long long)w;
@@ -201,8 +203,10 @@ strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe
   W.partial = h->partial;
   W.njb = njb;
   W.xfrag = reinterpret_cast<__half*>(wsb + o_xf);
-  W.gu = reinterpret_cast<float2*>(wsb + o_gu);
-  W.sgu = reinterpret_cast<float2*>(wsb + o_sgu);
+  W.hfrag = reinterpret_cast<__half*>(wsb + o_hf);
+  W.hsum = reinterpret_cast<float*>(wsb + o_hs);
+  W.shfrag = reinterpret_cast<__half*>(wsb + o_shf);
+  W.shsum = reinterpret_cast<float*>(wsb + o_shs);
   W.obuf = reinterpret_cast<float*>(wsb + o_ob);
   W.sbuf = reinterpret_cast<float*>(wsb + o_sb);
 
@@ -452,8 +456,10 @@ extern "C" strata_status strata_moe_window_forward_noalloc(strata_window* h, con
   const size_t o_cnt = w; w = align_up(w + (size_t)(d / 16) * 4, 256);
   const size_t o_done = w; w = align_up(w + (size_t)(E + 1) * 4, 256);
   const size_t o_part = w; w = align_up(w + (size_t)h->W.njb * kMaxRows * E * 4, 256);
-  const size_t o_gu = w; w = align_up(w + (size_t)kMaxEntries * F * 8, 256);
-  const size_t o_sgu = w; w = align_up(w + (size_t)kMaxRows * Fs * 8, 256);
+  const size_t o_hf = w; w = align_up(w + (size_t)kMaxEntries * 2 * F * 2, 256);
+  const size_t o_hs = w; w = align_up(w + (size_t)kMaxEntries * (F / 16) * 4, 256);
+  const size_t o_shf = w; w = align_up(w + (size_t)kMaxRows * 2 * Fs * 2, 256);
+  const size_t o_shs = w; w = align_up(w + (size_t)kMaxRows * (Fs / 16) * 4, 256);
   const size_t o_ob = w; w = align_up(w + (size_t)kMaxEntries * d * 4, 256);
   const size_t o_sb = w; w = align_up(w + (size_t)kMaxRows * d * 4, 256);
   if (w > (size_t)STRATA_NOALLOC_SCRATCH_BYTES) return STRATA_EUNSUPPORTED;
@@ -468,8 +474,10 @@ extern "C" strata_status strata_moe_window_forward_noalloc(strata_window* h, con
   W.counters = reinterpret_cast<int*>(base + o_cnt);
   W.done_gu = reinterpret_cast<int*>(base + o_done);
   W.partial = reinterpret_cast<float*>(base + o_part);
-  W.gu = reinterpret_cast<float2*>(base + o_gu);
-  W.sgu = reinterpret_cast<float2*>(base + o_sgu);
+  W.hfrag = reinterpret_cast<__half*>(base + o_hf);
+  W.hsum = reinterpret_cast<float*>(base + o_hs);
+  W.shfrag = reinterpret_cast<__half*>(base + o_shf);
+  W.shsum = reinterpret_cast<float*>(base + o_shs);
   W.obuf = reinterpret_cast<float*>(base + o_ob);
   W.sbuf = reinterpret_cast<float*>(base + o_sb);
   W.x = x;

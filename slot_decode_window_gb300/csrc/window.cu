@@ -601,8 +601,11 @@ __device__ __forceinline__ void split_tasks(const WindowBufs& W, SPlan& sp, bool
 }
 
 // Stage one group's activations into shared memory (all consumer threads).
-// Phase 0: copy the x fragments.  Phase 1: form h = silu(gu) * uu, its fp16
-// hi/lo fragments and its block sums.
+// Phases 0 and 2: copy x fragments (written by stage R or D0).  Phase 1: copy
+// h fragments (written by the gate/up epilogue) and form the block sums from
+// their 16-element partial sums.  The main-part copies are 16-byte cp.async
+// pieces, all in flight before the one wait.  Phase 3 (the dense o
+// projection) forms v's fragments here, since v is short.
 template <int BITS, int PHASE>
 __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan& sp, const KernelCfg& C, __half* bm,
                              __half* bs, bool is_shared, int R, int ent_off, int K, int ctid) {
@@ -611,10 +614,19 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
   const int nks = K / Fmt<BITS>::kKstep;
   const int nmk = (K / B + 15) / 16;
   const bool paired = R <= 4;
-  if (PHASE == 0 || PHASE == 2) {
+  const int nsets = paired ? 1 : 2;
+  const int ncols = paired ? 2 * R : R;
+  if constexpr (PHASE != 3) {
+    // the source of column col's part (hi or lo): one row of fragments
     const long long fh = frag_halves(K, nmk);
-    const int nsets = paired ? 1 : 2;
-    const int ncols = paired ? 2 * R : R;
+    auto row_base = [&](int r) -> const __half* {
+      if constexpr (PHASE == 1) {
+        return is_shared ? W.shfrag + (long long)r * 2 * L.Fs : W.hfrag + (long long)sp.entries[ent_off + r] * 2 * L.F;
+      } else {
+        const int xrow = (PHASE == 2 || is_shared) ? r : sp.entries[ent_off + r] / L.k;
+        return W.xfrag + xrow * fh;
+      }
+    };
     // main: 16-byte pieces (ks, c, plane) of each used column
     const int per_col = nks * 4 * (S / 8);
     for (int i = ctid; i < nsets * ncols * per_col; i += kConsumerThreads) {
@@ -622,44 +634,60 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
       const int set = cs / ncols, col = cs - set * ncols;
       const int r = paired ? (col >> 1) : col;
       const int part = paired ? (col & 1) : set;
-      const int xrow = (PHASE == 2 || is_shared) ? r : sp.entries[ent_off + r] / L.k;
       const int ks = rem / (4 * (S / 8)), cp = rem - ks * 4 * (S / 8);
       const int c = cp / (S / 8), p = cp - c * (S / 8);
-      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(W.xfrag + xrow * fh + (long long)part * K + ks * 4 * S +
-                                                            c * S + p * 8));
-      *reinterpret_cast<uint4*>(bm + set * C.bmain_halves + bmain_off<BITS>(ks, p, col, c)) = v;
+      cp_async16(bm + set * C.bmain_halves + bmain_off<BITS>(ks, p, col, c),
+                 row_base(r) + (long long)part * K + ks * 4 * S + c * S + p * 8);
     }
-    // sums: 8-byte pieces (mk, c)
-    for (int i = ctid; i < nsets * ncols * nmk * 4; i += kConsumerThreads) {
-      const int cs = i / (nmk * 4), rem = i - cs * nmk * 4;
-      const int set = cs / ncols, col = cs - set * ncols;
-      const int r = paired ? (col >> 1) : col;
-      const int part = paired ? (col & 1) : set;
-      const int xrow = (PHASE == 2 || is_shared) ? r : sp.entries[ent_off + r] / L.k;
-      const int mk = rem >> 2, c = rem & 3;
-      const uint2 v = __ldcg(reinterpret_cast<const uint2*>(W.xfrag + xrow * fh + 2LL * K +
-                                                            (long long)part * 16 * nmk + mk * 16 + c * 4));
-      *reinterpret_cast<uint2*>(bs + set * C.bsum_halves + (mk * 8 + col) * 16 + c * 4) = v;
+    if constexpr (PHASE == 1) {
+      // block sums from the 16-element partial sums, split into hi/lo
+      constexpr int kParts = B / 16;
+      for (int i = ctid; i < R * (K / B); i += kConsumerThreads) {
+        const int r = i / (K / B), blk = i - r * (K / B);
+        const float* hs = is_shared ? W.shsum + (long long)r * (L.Fs / 16)
+                                    : W.hsum + (long long)sp.entries[ent_off + r] * (L.F / 16);
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < kParts; ++j) sum += __ldcg(hs + blk * kParts + j);
+        __half hi, lo;
+        split_hi_lo(sum, hi, lo);
+        const int spos = frag_sum_pos(blk);
+        const int mk = spos >> 4, c = (spos >> 2) & 3, slot = spos & 3;
+        const int o = mk * 128 + c * 4 + slot;
+        if (paired) {
+          bs[o + (2 * r) * 16] = hi;
+          bs[o + (2 * r + 1) * 16] = lo;
+        } else {
+          bs[o + r * 16] = hi;
+          bs[C.bsum_halves + o + r * 16] = lo;
+        }
+      }
+    } else {
+      // sums: 8-byte pieces (mk, c)
+      for (int i = ctid; i < nsets * ncols * nmk * 4; i += kConsumerThreads) {
+        const int cs = i / (nmk * 4), rem = i - cs * nmk * 4;
+        const int set = cs / ncols, col = cs - set * ncols;
+        const int r = paired ? (col >> 1) : col;
+        const int part = paired ? (col & 1) : set;
+        const int mk = rem >> 2, c = rem & 3;
+        const uint2 v = __ldcg(reinterpret_cast<const uint2*>(row_base(r) + 2LL * K + (long long)part * 16 * nmk +
+                                                              mk * 16 + c * 4));
+        *reinterpret_cast<uint2*>(bs + set * C.bsum_halves + (mk * 8 + col) * 16 + c * 4) = v;
+      }
     }
+    cp_async_wait_all();
   } else {
-    // one element per thread and step; a warp covers 32 consecutive elements of
-    // one row (K is a multiple of 64), so block sums come from lane shuffles.
-    // Phase 1: h = silu(gu) * uu.  Phase 3: h = v (K = dkv); its block sums are
-    // written for every block of the broadcast input that repeats that v block.
+    // v (K = dkv): one element per thread and step; a warp covers 32
+    // consecutive elements of one row (K is a multiple of 64), so block sums
+    // come from lane shuffles, written for every block of the broadcast input
+    // that repeats that v block
     for (int i0 = 0; i0 < R * K; i0 += kConsumerThreads) {
       const int i = i0 + ctid;
       const bool in = i < R * K;
       const int r = in ? i / K : 0, f = in ? i - r * K : 0;
       float h = 0.f;
       if (in) {
-        if constexpr (PHASE == 3) {
-          h = __ldcg(W.v + (long long)r * L.dkv + f);
-        } else {
-          const float2* src =
-              is_shared ? W.sgu + (long long)r * L.Fs : W.gu + (long long)sp.entries[ent_off + r] * L.F;
-          const float2 gu = __ldcg(src + f);
-          h = silu_f32(gu.x) * gu.y;
-        }
+        h = __ldcg(W.v + (long long)r * L.dkv + f);
         int off;
         float fac;
         frag_main_pos<BITS>(f, off, fac);
@@ -682,12 +710,11 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
         __half hi, lo;
         split_hi_lo(s, hi, lo);
         // v block vb = (kv group, block in head) -> broadcast blocks (group * G + head) * bph + j
-        const int bph = PHASE == 3 ? (1 << L.kph_log2) * Fmt<BITS>::kBlocksPerKstep : 1;
-        const int ncopy = PHASE == 3 ? 1 << (L.kpg_log2 - L.kph_log2) : 1;
+        const int bph = (1 << L.kph_log2) * Fmt<BITS>::kBlocksPerKstep;
+        const int ncopy = 1 << (L.kpg_log2 - L.kph_log2);
         const int vb = f / B, grp = vb / bph, j = vb - grp * bph;
         for (int hc = 0; hc < ncopy; ++hc) {
-          const int beta = PHASE == 3 ? (grp * ncopy + hc) * bph + j : vb;
-          const int spos = frag_sum_pos(beta);
+          const int spos = frag_sum_pos((grp * ncopy + hc) * bph + j);
           const int mk = spos >> 4, c = (spos >> 2) & 3, slot = spos & 3;
           const int o = mk * 128 + c * 4 + slot;
           if (paired) {
@@ -918,9 +945,26 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
           gv += frag_pick(rb[(m * kWPS + w) * 32 + src_lane], idx, paired);
           uv += frag_pick(rb[((kMT + m) * kWPS + w) * 32 + src_lane], idx, paired);
         }
+        // h = silu(gate) * up, stored as the down phase's activation fragments:
+        // fp16 hi/lo parts at the element's fragment slot, and the sum of the 16
+        // elements of this sub-tile (held by 16 consecutive lanes: i % 16 == row)
         const int f = (tk.tile + m) * 16 + row;
-        float2* dst = tk.shared ? W.sgu + (long long)r * L.Fs : W.gu + (long long)sp.entries[ent_off + r] * L.F;
-        dst[f] = make_float2(gv, uv);
+        const float h = silu_f32(gv) * uv;
+        const int Kh = tk.shared ? L.Fs : L.F;
+        const long long hrow = tk.shared ? r : sp.entries[ent_off + r];
+        __half* hb = (tk.shared ? W.shfrag : W.hfrag) + hrow * 2 * Kh;
+        int off;
+        float fac;
+        frag_main_pos<BITS>(f, off, fac);
+        __half hi, lo;
+        split_hi_lo(h * fac, hi, lo);
+        hb[off] = hi;
+        hb[Kh + off] = lo;
+        const unsigned half_mask = 0xffffu << (lane & 16);
+        float ps = h;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) ps += __shfl_xor_sync(half_mask, ps, o);
+        if (row == 0) (tk.shared ? W.shsum : W.hsum)[hrow * (Kh / 16) + f / 16] = ps;
       }
     } else {
       for (int i = eo; i < NS * 16 * R; i += kConsumerThreads) {

@@ -42,13 +42,13 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row(B):
 
 
 def test_noalloc_rejects_a_shape_beyond_its_scratch(B):
-    # F = 8192: the gate/up results alone (64 entries x 8192 x 8 B) fill the
-    # 4 MiB array
-    spec = wlm.MoESpec(4096, 1, 1, 8192, 0, 4, 32)
+    # d = F = 8192: the down outputs (64 entries x 8192 x 4 B) and the h
+    # fragments (64 x 2 x 8192 x 2 B) together exceed the 4 MiB array
+    spec = wlm.MoESpec(8192, 1, 1, 8192, 0, 4, 32)
     layer = wlm.make_moe_layer(spec, seed=0, cfg_id=78, device="cuda")
     win = B.Window(layer, max_rows=4)
     assert win.info().workspace_bytes > B.NOALLOC_SCRATCH_BYTES
-    x = torch.zeros(1, 4096, device="cuda")
+    x = torch.zeros(1, 8192, device="cuda")
     y = torch.zeros_like(x)
     assert B.strata_moe_window_forward_noalloc(win.handle, x.data_ptr(), 1, y.data_ptr()) == B.STRATA_EUNSUPPORTED
     assert B.strata_moe_window_forward_noalloc(win.handle, x.data_ptr(), 0, y.data_ptr()) == B.STRATA_EINVAL
