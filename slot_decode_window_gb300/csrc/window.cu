@@ -1179,12 +1179,14 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
     p0.ntask_e = tiles_e / p0.mt;
     split_tasks(W, sp, has_shared, p0, lane);
   } else if (warp == 1) {
-    // down: as many row tiles per task as keep >= 3 tasks per CTA (up to 4)
+    // down: as many row tiles per task (up to 4) as keep >= 1 task per CTA;
+    // with few rows a down task is short, and its fixed cost (wait, sync,
+    // epilogue) outweighs the finer balance of narrower tasks
     PhaseTasks& p1 = sp.pt[1];
     const int tiles_g = L.d / 16;
     const long long all1 = (long long)((has_shared ? 1 : 0) + nd) * tiles_g;
     int mt = C.ph[1].max_sub;
-    while (mt > 1 && (tiles_g % mt != 0 || all1 / mt < 3LL * gridDim.x)) mt >>= 1;
+    while (mt > 1 && (tiles_g % mt != 0 || all1 / mt < (long long)gridDim.x)) mt >>= 1;
     p1.mt = mt;
     p1.ntask_s = has_shared ? tiles_g / mt : 0;
     p1.ntask_e = tiles_g / mt;
