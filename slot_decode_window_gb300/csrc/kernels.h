@@ -4,7 +4,7 @@
 
 namespace strata {
 
-constexpr int kRouterCols = 256;  // columns per router partial-logit chunk
+constexpr int kRouterCols = 512;  // columns per router partial-logit chunk
 
 // Shared-memory plan of the window kernel for one layer shape.
 KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit);

@@ -48,6 +48,52 @@ constexpr int kMaxSub = 4;  // sub-tiles per task
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr long long kWaitCycles = 1LL << 31;  // about a second at GB300 clocks
 
+// Stage timestamps for timing builds (-DSTRATA_STAMPS): one lane of the CTA
+// records %globaltimer at stage boundaries into g_stamps[cta][slot].  The
+// default build compiles these to nothing.
+#ifdef STRATA_STAMPS
+}  // namespace
+__device__ unsigned long long g_stamps[1024][20];
+namespace {
+__device__ __forceinline__ void stamp(int slot) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  g_stamps[blockIdx.x][slot] = t;
+}
+#define STAMP(tid_, slot_) \
+  do {                     \
+    if (threadIdx.x == (tid_)) stamp(slot_); \
+  } while (0)
+// per-task trace: g_trace[cta][phase][task slot][event]
+__device__ unsigned long long g_trace[1024][2][32][4];
+__device__ unsigned long long g_ptrace[1024][2][64];  // producer: chunk issue times
+__device__ __forceinline__ void trace(int phase, int slot, int ev) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  if (slot < 32) g_trace[blockIdx.x][phase][slot][ev] = t;
+}
+#define TRACE(tid_, ph_, slot_, ev_) \
+  do {                               \
+    if (threadIdx.x == (tid_)) trace(ph_, slot_, ev_); \
+  } while (0)
+#define PTRACE(ph_, n_)                                                   \
+  do {                                                                    \
+    unsigned long long t_;                                                \
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                \
+    if ((n_) < 64) g_ptrace[blockIdx.x][ph_][n_] = t_;                    \
+  } while (0)
+#else
+#define TRACE(tid_, ph_, slot_, ev_) \
+  do {                               \
+  } while (0)
+#define PTRACE(ph_, n_) \
+  do {                  \
+  } while (0)
+#define STAMP(tid_, slot_) \
+  do {                     \
+  } while (0)
+#endif
+
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigned* err, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
@@ -308,41 +354,124 @@ __device__ __noinline__ void row_rinv(const float* x, int T, int d, float* s_rin
   __syncthreads();
 }
 
+// Sum of v[0..7] (one value per row t) over the 32 lanes of a warp, by
+// halving: after the exchanges across lane bits 4, 3 and 2 every lane holds a
+// partial sum of one row, t = 4*b4 + 2*b3 + b2 (its lane bits), and two more
+// exchanges complete it.  9 shuffles instead of 8 x 5.
+__device__ __forceinline__ float warp_sum8(float (&v)[kMaxRows], int lane) {
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b4 ? v[i] : v[i + 4], keep = b4 ? v[i + 4] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b3 ? v[i] : v[i + 2], keep = b3 ? v[i + 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  {
+    const float send = b2 ? v[0] : v[1], keep = b2 ? v[1] : v[0];
+    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+  return v[0];
+}
+
+// Stage R.  The d columns are cut into njb chunks of kRouterCols; the CTAs
+// are dealt out over the chunks (CTA c takes chunk c mod njb, together with
+// the other CTAs of that chunk), so each CTA stages its chunk of the T rows of
+// x in shared memory once.  Its warps then take the chunk's experts in turn:
+// partial[jb][t][e] = sum over the chunk of Wr[e][j] x[t][j] (times 1/RMS of
+// row t in a decoder layer).  Last, the CTA writes its share of the chunk's
+// activation fragments (fp16 hi/lo and block sums) from the staged rows.
 template <int BITS>
-__device__ __noinline__ void router_stage(const LayerDev& L, const WindowBufs& W) {
-  const int T = W.T, d = L.d, E = L.E;
+__device__ __noinline__ void router_stage(const LayerDev& L, const WindowBufs& W, float* xs) {
+  constexpr int B = Fmt<BITS>::kBlock;
+  const int T = W.T, d = L.d, E = L.E, njb = W.njb, G = gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
-  const int npairs = E * W.njb;
-  for (int p = warp * gridDim.x + blockIdx.x; p < npairs; p += gridDim.x * nwarps) {
-    const int e = p % E, jb = p / E;  // pairs spread over all CTAs
+  const bool spread = G >= njb;  // several CTAs per chunk (always, for the shapes here)
+  const int nmk = (d / B + 15) / 16;
+  const long long fh = frag_halves(d, nmk);
+  for (int jb = spread ? (int)blockIdx.x % njb : (int)blockIdx.x; jb < njb; jb += spread ? njb : G) {
+    const int cpc = spread ? G / njb + (jb < G % njb ? 1 : 0) : 1;  // CTAs on this chunk
+    const int ci = spread ? (int)blockIdx.x / njb : 0;              // this CTA among them
     const int j0 = jb * kRouterCols, ncol = min(kRouterCols, d - j0);
-    float acc[kMaxRows];
+    const int nq = ncol / 4;
+    __syncthreads();  // xs is free (a previous chunk of this loop is done)
+    for (int i = threadIdx.x; i < T * nq; i += blockDim.x) {
+      const int t = i / nq, q = i - t * nq;
+      cp_async16(xs + t * kRouterCols + 4 * q, W.x + (long long)t * d + j0 + 4 * q);
+    }
+    const int e0 = (int)((long long)E * ci / cpc), e1 = (int)((long long)E * (ci + 1) / cpc);
+    // a warp's router row segment, loaded a row ahead (the first one while the
+    // rows of x are still landing)
+    constexpr int kJ = kRouterCols / 128;
+    float4 w[kJ];
+    auto load_w = [&](int e) {
+      const float* wr = L.router_w + (long long)e * d + j0;
 #pragma unroll
-    for (int t = 0; t < kMaxRows; ++t) acc[t] = 0.f;
-    const float* wr = L.router_w + (long long)e * d + j0;
-    for (int j = lane * 4; j < ncol; j += 128) {
-      const float4 w4 = *reinterpret_cast<const float4*>(wr + j);
+      for (int i = 0; i < kJ; ++i) {
+        const int j = lane * 4 + 128 * i;
+        w[i] = (e < e1 && j < ncol) ? __ldcs(reinterpret_cast<const float4*>(wr + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    };
+    load_w(e0 + warp);
+    cp_async_wait_all();
+    __syncthreads();
+    for (int e = e0 + warp; e < e1; e += nwarps) {
+      float acc[kMaxRows];
 #pragma unroll
-      for (int t = 0; t < kMaxRows; ++t) {
-        if (t < T) {
-          const float4 x4 = __ldg(reinterpret_cast<const float4*>(W.x + (long long)t * d + j0 + j));
-          acc[t] = fmaf(w4.x, x4.x, acc[t]);
-          acc[t] = fmaf(w4.y, x4.y, acc[t]);
-          acc[t] = fmaf(w4.z, x4.z, acc[t]);
-          acc[t] = fmaf(w4.w, x4.w, acc[t]);
+      for (int t = 0; t < kMaxRows; ++t) acc[t] = 0.f;
+#pragma unroll
+      for (int i = 0; i < kJ; ++i) {
+        const int j = lane * 4 + 128 * i;
+        if (j < ncol) {
+#pragma unroll
+          for (int t = 0; t < kMaxRows; ++t) {
+            if (t < T) {
+              const float4 x4 = *reinterpret_cast<const float4*>(xs + t * kRouterCols + j);
+              acc[t] = fmaf(w[i].x, x4.x, acc[t]);
+              acc[t] = fmaf(w[i].y, x4.y, acc[t]);
+              acc[t] = fmaf(w[i].z, x4.z, acc[t]);
+              acc[t] = fmaf(w[i].w, x4.w, acc[t]);
+            }
+          }
         }
       }
+      load_w(e + nwarps);
+      const float v = warp_sum8(acc, lane);
+      const int t = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+      if ((lane & 3) == 0 && t < T)
+        W.partial[((long long)jb * kMaxRows + t) * E + e] = W.rinv ? v * W.rinv[t] : v;
     }
+    // this CTA's share of the chunk's activation fragments: units of 32
+    // consecutive elements of one row (whole blocks), one per warp
+    const int upr = ncol / 32, nu = T * upr;
+    for (int u = ci + cpc * warp; u < nu; u += cpc * nwarps) {
+      const int t = u / upr, jj = (u - t * upr) * 32 + lane, j = j0 + jj;
+      const float v = W.rinv ? xs[t * kRouterCols + jj] * W.rinv[t] : xs[t * kRouterCols + jj];
+      __half* base = W.xfrag + t * fh;
+      int off;
+      float f;
+      frag_main_pos<BITS>(j, off, f);
+      __half hi, lo;
+      split_hi_lo(v * f, hi, lo);
+      base[off] = hi;
+      base[d + off] = lo;
+      float sm = v;
 #pragma unroll
-    for (int t = 0; t < kMaxRows; ++t) {
-      float v = acc[t];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == t && t < T) W.partial[((long long)jb * kMaxRows + t) * E + e] = W.rinv ? v * W.rinv[t] : v;
+      for (int o = B / 2; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+      if ((j % B) == 0) {
+        split_hi_lo(sm, hi, lo);
+        const int soff = frag_sum_pos(j / B);
+        base[2 * d + soff] = hi;
+        base[2 * d + nmk * 16 + soff] = lo;
+      }
     }
   }
-  write_x_frags<BITS>(L, W);
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < d / 16; i += blockDim.x) W.counters[i] = 0;
     for (int i = threadIdx.x; i <= E; i += blockDim.x) W.done_gu[i] = 0;
@@ -382,23 +511,38 @@ __device__ __noinline__ void compute_plan(const LayerDev& L, const WindowBufs& W
   const int T = W.T, E = L.E, k = L.k, njb = W.njb;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool pub = blockIdx.x == 0;
-  // 1. logits: the column-chunk partials summed in chunk order, loads batched
-  for (int i = tid; i < T * E; i += blockDim.x) {
-    const int t = i / E, e = i - t * E;
-    const float* pp = W.partial + (long long)t * E + e;
-    float v = 0.f;
-    for (int b0 = 0; b0 < njb; b0 += 16) {
-      float part[16];
+  // 1. logits: the column-chunk partials summed in chunk order; a thread
+  //    issues the loads of up to kU logits before it sums any of them
+  {
+    constexpr int kU = 4, kB = 8;
+    const int n = T * E;
+    for (int i0 = tid; i0 < n; i0 += kU * blockDim.x) {
+      float v[kU];
 #pragma unroll
-      for (int b = 0; b < 16; ++b)
-        part[b] = (b0 + b < njb) ? __ldcg(pp + (long long)(b0 + b) * kMaxRows * E) : 0.f;
+      for (int u = 0; u < kU; ++u) v[u] = 0.f;
+      for (int b0 = 0; b0 < njb; b0 += kB) {
+        float part[kU][kB];
 #pragma unroll
-      for (int b = 0; b < 16; ++b) v += part[b];
+        for (int u = 0; u < kU; ++u) {
+          const int i = i0 + u * blockDim.x;
+#pragma unroll
+          for (int b = 0; b < kB; ++b)
+            part[u][b] = (i < n && b0 + b < njb) ? __ldcg(W.partial + (long long)(b0 + b) * kMaxRows * E + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+          for (int b = 0; b < kB; ++b) v[u] += part[u][b];
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * blockDim.x;
+        if (i < n) lg[i] = L.router_b ? v[u] + L.router_b[i % E] : v[u];
+      }
     }
-    if (L.router_b) v += L.router_b[e];
-    lg[t * E + e] = v;
   }
   __syncthreads();
+  STAMP(0, 17);
   // 2. top-k by logit (descending, ties -> lower expert index) and the fp32
   //    softmax weights of the chosen experts; warp t owns row t, its logits in
   //    registers (E <= 256: eight per lane)
@@ -456,6 +600,7 @@ __device__ __noinline__ void compute_plan(const LayerDev& L, const WindowBufs& W
     }
   }
   __syncthreads();
+  STAMP(0, 18);
   // 3. grouping: entries ordered by expert, then by entry index.  Warps 0 and 1
   //    hold entries 0..31 and 32..63; match_any gives each entry its rank among
   //    the same expert's entries of its warp and each warp's per-expert count.
@@ -783,6 +928,43 @@ struct TaskWalk {
 // ---------------------------------------------------------------------------
 // producer: one thread streams every task's k-chunks, phase 0 then phase 1
 // ---------------------------------------------------------------------------
+// The packed matrix sub-tile s of a task reads (phase 0: kMT gate tiles, then
+// kMT up tiles; the other phases: kMT tiles of one matrix): its base and the
+// bytes of one expert's matrix.  Values, not references: a reference into the
+// kernel's parameter struct would force a local copy of the whole struct.
+struct MatRef {
+  const uint8_t* base;
+  long long mat_bytes;
+};
+__device__ __forceinline__ MatRef mat_ref(const PackedMat& M) { return MatRef{M.base, M.mat_bytes}; }
+
+template <int PHASE, int kMT>
+__device__ __forceinline__ MatRef task_mat(const LayerDev& L, bool shared, int s) {
+  if constexpr (PHASE == 0) {
+    const bool up = s >= kMT;
+    const uint8_t* b = up ? (shared ? L.sup.base : L.up.base) : (shared ? L.sgate.base : L.gate.base);
+    const long long mb = up ? (shared ? L.sup.mat_bytes : L.up.mat_bytes)
+                            : (shared ? L.sgate.mat_bytes : L.gate.mat_bytes);
+    return MatRef{b, mb};
+  } else if constexpr (PHASE == 1) {
+    return MatRef{shared ? L.sdown.base : L.down.base, shared ? L.sdown.mat_bytes : L.down.mat_bytes};
+  } else if constexpr (PHASE == 2) {
+    return mat_ref(L.qkv);
+  } else {
+    return mat_ref(L.o);
+  }
+}
+
+template <int BITS, int PHASE>
+__device__ __forceinline__ int task_k(const LayerDev& L, bool shared) {
+  return PHASE == 0 ? L.d : PHASE == 1 ? (shared ? L.Fs : L.F) : PHASE == 2 ? L.d : L.dq;
+}
+
+template <int BITS>
+__device__ __forceinline__ int tile_bytes_of(int K) {
+  return (K / Fmt<BITS>::kKstep) * Fmt<BITS>::kChunk + ((K / Fmt<BITS>::kBlock + 15) / 16) * 512;
+}
+
 template <int BITS, int PHASE, int NS>
 __device__ bool produce(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, const SPlan& sp, const Ring& rg,
                         RingPos& rp) {
@@ -790,6 +972,9 @@ __device__ bool produce(const LayerDev& L, const WindowBufs& W, const KernelCfg&
   const PhaseCfg& P = C.ph[PHASE];
   const PhaseTasks& pt = sp.pt[PHASE];
   const bool has_shared = L.Fs > 0;
+  // the ring was last written through the generic proxy (staged router rows,
+  // plan scratch): order that before the bulk copies
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   TaskWalk tw;
   if (pt.t0 < pt.t1) tw.start(pt.t0, pt, has_shared, sp);
   for (int task = pt.t0; task < pt.t1; ++task, tw.next(pt, has_shared, sp)) {
@@ -799,25 +984,37 @@ __device__ bool produce(const LayerDev& L, const WindowBufs& W, const KernelCfg&
       *rg.abort_flag = 1;
       return false;
     }
-    const int K = PHASE == 0 ? L.d : PHASE == 1 ? (tk.shared ? L.Fs : L.F) : PHASE == 2 ? L.d : L.dq;
-    const int nks = K / Fmt<BITS>::kKstep, nmk = (K / Fmt<BITS>::kBlock + 15) / 16;
-    const int tbytes = nks * Fmt<BITS>::kChunk + nmk * 512;
+    const int K = task_k<BITS, PHASE>(L, tk.shared);
+    const int nks = K / Fmt<BITS>::kKstep;
+    const int tbytes = tile_bytes_of<BITS>(K);
     const int kv = (PHASE == 1 && tk.shared) ? 1 : 0;
     for (int ch = 0; ch < P.nchunks; ++ch) {
       const int ks0 = P.cks[kv][ch], ks1 = P.cks[kv][ch + 1];
       const int mk0 = P.cmk[kv][ch], mk1 = P.cmk[kv][ch + 1];
       const int stage = rp.stage;
       if (rp.n >= C.nstages && !wait_bar(&rg.empty[stage], rp.parity ^ 1u, W.err, rg.abort_flag)) return false;
+      if (PHASE < 2) PTRACE(PHASE, (task - pt.t0) * P.nchunks + ch);
       const uint32_t cbytes = (uint32_t)((ks1 - ks0) * Fmt<BITS>::kChunk), mbytes = (uint32_t)((mk1 - mk0) * 512);
-      mbar_arrive_expect_tx(&rg.full[stage], NS * (cbytes + mbytes));
       uint8_t* dst = rg.base + (size_t)stage * C.stage_bytes;
+      if (P.nchunks == 1 && tbytes == P.sub_stride) {
+        // whole tiles, laid out in the stage as in memory: one copy per run
+        // of consecutive tiles (phase 0: the gate run, then the up run)
+        mbar_arrive_expect_tx(&rg.full[stage], NS * tbytes);
+#pragma unroll
+        for (int r = 0; r < (PHASE == 0 ? 2 : 1); ++r) {
+          const MatRef M = task_mat<PHASE, kMT>(L, tk.shared, r * kMT);
+          const uint8_t* src =
+              M.base + (tk.shared ? 0LL : (long long)tk.expert * M.mat_bytes) + (long long)tk.tile * tbytes;
+          bulk_g2s(dst + r * kMT * P.sub_stride, src, (uint32_t)(kMT * tbytes), &rg.full[stage]);
+        }
+        rp.advance(C.nstages);
+        continue;
+      }
+      mbar_arrive_expect_tx(&rg.full[stage], NS * (cbytes + mbytes));
 #pragma unroll
       for (int s = 0; s < NS; ++s) {
         const bool up = PHASE == 0 && s >= kMT;
-        const PackedMat& M = PHASE == 0   ? (up ? (tk.shared ? L.sup : L.up) : (tk.shared ? L.sgate : L.gate))
-                             : PHASE == 1 ? (tk.shared ? L.sdown : L.down)
-                             : PHASE == 2 ? L.qkv
-                                          : L.o;
+        const MatRef M = task_mat<PHASE, kMT>(L, tk.shared, s);
         const int tile = tk.tile + (up ? s - kMT : s);
         const uint8_t* src =
             M.base + (tk.shared ? 0LL : (long long)tk.expert * M.mat_bytes) + (long long)tile * tbytes;
@@ -895,14 +1092,17 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
           }
         }
         consumer_sync();
+        if (cur == -2) STAMP(0, 6);
       }
       // the previous task's barrier guarantees no warp still reads the old fragments
       load_group_B<BITS, PHASE>(L, W, sp, C, bm, bs, tk.shared, R, ent_off, PHASE == 3 ? L.dkv : K, tid);
       consumer_sync();
+      if (PHASE == 1 && cur == -2) STAMP(0, 7);
       cur = tk.group;
     }
     const int kv = (PHASE == 1 && tk.shared) ? 1 : 0;
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
+    if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 0);
     for (int ch = 0; ch < P.nchunks; ++ch) {
       const int ks0 = P.cks[kv][ch], ks1 = P.cks[kv][ch + 1];
       const int mk0 = P.cmk[kv][ch], mk1 = P.cmk[kv][ch + 1];
@@ -911,6 +1111,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
       const int m0 = (kg * nm) / kWPS, m1 = ((kg + 1) * nm) / kWPS;
       const int stage = rp.stage;
       if (wait_bar(&rg.full[stage], rp.parity, W.err, rg.abort_flag)) {
+        if (PHASE < 2 && ch == 0) TRACE(0, PHASE, task - pt.t0, 1);
         const uint8_t* st = rg.base + (size_t)stage * C.stage_bytes + sub * P.sub_stride;
         constexpr bool kVmap = PHASE == 3;
         if (paired)
@@ -924,10 +1125,12 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
       if (lane == 0) mbar_arrive(&rg.empty[stage]);
       rp.advance(C.nstages);
     }
+    if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 2);
     float4* rb = red + buf * (kConsumerWarps * 32);
     rb[warp * 32 + lane] = make_float4(fmaf(acc[0], kDqUnscale, accm[0]), fmaf(acc[1], kDqUnscale, accm[1]),
                                        fmaf(acc[2], kDqUnscale, accm[2]), fmaf(acc[3], kDqUnscale, accm[3]));
     consumer_sync();
+    if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 3);
 
     // ---------------- epilogue: cross-warp sums in a fixed order ----------------
     // outputs on consecutive threads of one or two warps, rotating with the task,
@@ -1163,6 +1366,7 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // P: the routing plan (the ring is free until the producer starts: logits scratch)
   compute_plan(L, W, sp, reinterpret_cast<float*>(m.ring));
+  STAMP(0, 3);
   const int nd = sp.nd;
   if (nd < 0 || nd > L.E) {
     if (tid == 0) atomicOr(W.err, kErrIndex);
@@ -1193,34 +1397,49 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
     split_tasks(W, sp, has_shared, p1, lane);
   }
   __syncthreads();
+#ifdef STRATA_STAMPS
+  if (tid == 0) {
+    g_stamps[blockIdx.x][13] = (unsigned long long)(sp.pt[0].t1 - sp.pt[0].t0);
+    g_stamps[blockIdx.x][14] = (unsigned long long)(sp.pt[1].t1 - sp.pt[1].t0);
+    g_stamps[blockIdx.x][15] = (unsigned long long)(sp.pt[0].mt * 100 + sp.pt[1].mt);
+  }
+#endif
+  STAMP(0, 4);
 
   const int ns0 = 2 * sp.pt[0].mt, ns1 = sp.pt[1].mt;
   if (warp == kConsumerWarps) {
     // ---------------- producer ----------------
     if (lane == 0) {
       const bool ok = ns0 == 4 ? produce<BITS, 0, 4>(L, W, C, sp, rg, rp) : produce<BITS, 0, 2>(L, W, C, sp, rg, rp);
+      STAMP(kConsumerThreads, 11);
       if (ok) {
         if (ns1 == 4) produce<BITS, 1, 4>(L, W, C, sp, rg, rp);
         else if (ns1 == 2) produce<BITS, 1, 2>(L, W, C, sp, rg, rp);
         else produce<BITS, 1, 1>(L, W, C, sp, rg, rp);
       }
+      STAMP(kConsumerThreads, 12);
       if (*rg.abort_flag) drain_ring(rg, C, rp);
     }
     return true;
   }
   if (ns0 == 4) consume<BITS, 0, 4>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
   else consume<BITS, 0, 2>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+  STAMP(0, 5);
   const bool slices = W.T < kGridCombineRows;  // else the caller combines after a grid barrier
   if (ns1 == 4) {
     consume<BITS, 1, 4>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+    STAMP(0, 8);
     if (slices) combine<4>(L, W, sp);
   } else if (ns1 == 2) {
     consume<BITS, 1, 2>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+    STAMP(0, 8);
     if (slices) combine<2>(L, W, sp);
   } else {
     consume<BITS, 1, 1>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+    STAMP(0, 8);
     if (slices) combine<1>(L, W, sp);
   }
+  STAMP(0, 9);
   return true;
 }
 
@@ -1271,16 +1490,25 @@ __global__ void __launch_bounds__(kExpertThreads, 1) window_kernel(LayerDev L, W
   const Ring rg{m.ring, m.full, m.empty, &s_abort};
   init_cta(C, m, &s_abort);
   for (int i = threadIdx.x; i < 2 * kMaxExperts; i += blockDim.x) (&sp.wcnt[0][0])[i] = 0;
+  STAMP(0, 0);
 
   // R: router partial logits, x fragments; then every CTA waits for all
-  router_stage<BITS>(L, W);
+  router_stage<BITS>(L, W, reinterpret_cast<float*>(m.ring));
+  STAMP(0, 1);
+#ifdef STRATA_STAMPS
+  __syncthreads();
+  STAMP(0, 19);
+#endif
   if (!grid_barrier(W, &sp.ok)) return;  // timed out: the error word says so
+  STAMP(0, 2);
   RingPos rp;
   int buf = 0;
   if (!moe_block<BITS>(L, W, C, sp, rg, m, rp, buf)) return;
   if (W.T >= kGridCombineRows) {
     if (!grid_barrier(W, &sp.ok) || s_abort) return;
+    STAMP(0, 10);
     combine_all(L, W);
+    STAMP(0, 16);
   }
 }
 
@@ -1348,7 +1576,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1)
     }
     __syncthreads();
     row_rinv(sW.x, sW.T, L.d, s_rinv);
-    router_stage<BITS>(L, sW);
+    router_stage<BITS>(L, sW, reinterpret_cast<float*>(m.ring));
     if (!grid_barrier(sW, &sp.ok)) return;
     if (!moe_block<BITS>(L, sW, C, sp, rg, m, rp, buf)) return;
     if (sW.T >= kGridCombineRows) {
@@ -1513,3 +1741,20 @@ cudaError_t launch_stack(const LayerDev* layers, int n_layers, int bits, const W
 }
 
 }  // namespace strata
+
+#ifdef STRATA_STAMPS
+// Timing builds only: copy the stage timestamps of the first n CTAs to host.
+extern "C" int strata_probe_stamps(void* host, int n) {
+  return (int)cudaMemcpyFromSymbol(host, strata::g_stamps, (size_t)n * 20 * sizeof(unsigned long long));
+}
+extern "C" int strata_probe_trace(void* host, int n) {
+  return (int)cudaMemcpyFromSymbol(host, strata::g_trace, (size_t)n * 2 * 32 * 4 * sizeof(unsigned long long));
+}
+extern "C" int strata_probe_ptrace(void* host, int n) {
+  return (int)cudaMemcpyFromSymbol(host, strata::g_ptrace, (size_t)n * 2 * 64 * sizeof(unsigned long long));
+}
+extern "C" int strata_probe_trace_clear() {
+  static unsigned long long zero[1024 * 2 * 32 * 4];
+  return (int)cudaMemcpyToSymbol(strata::g_trace, zero, sizeof(zero));
+}
+#endif
