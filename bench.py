@@ -50,6 +50,7 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=20.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-stack", action="store_true", help="skip the 48-layer stack measurement")
+    p.add_argument("--no-workloads", action="store_true", help="skip the zipf and lowbit layer measurements")
     p.add_argument("--stack-steps", type=int, default=30)
     p.add_argument("--stack-layers", type=int, default=2, help="layers of the stack in --mode stack")
     p.add_argument("--mode", choices=("full", "windows", "stack"), default="full",
@@ -121,6 +122,17 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------------------------
 # helpers
+
+
+def flush_and_hold(flush):
+    """Evict L2 (a memset of 2x its size), then keep the GPU busy for ~25 us
+    with a spin kernel, so that the host enqueues the start event and the
+    timed launch before the GPU reaches them (no host latency inside the
+    device-timed region)."""
+    import torch
+    flush.zero_()
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(50000)
 
 
 def measured_peak_hbm():
@@ -324,7 +336,7 @@ def run_ours(args, rank, world, local_rank):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         t0 = time.perf_counter()
         for i in range(steps):
-            flush.zero_()
+            flush_and_hold(flush)
             evs[i][0].record(stream)
             win.forward(X[T][i % N_WINDOWS], Y[:T])
             evs[i][1].record(stream)
@@ -373,7 +385,7 @@ def run_ours(args, rank, world, local_rank):
     g_ms = []
     for i in range(min(args.steps, 500)):
         xg.copy_(X[T][i % N_WINDOWS])
-        flush.zero_()
+        flush_and_hold(flush)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         win.forward_graph(xg, yg)
@@ -390,7 +402,7 @@ def run_ours(args, rank, world, local_rank):
     k_ms = []
     wb = 0.0
     for i in range(prof_steps):
-        flush.zero_()
+        flush_and_hold(flush)
         win.forward(X[T][i % N_WINDOWS], Y[:T])
         k_ms.append(win.timings())
         wb += window_bytes(T, i % N_WINDOWS)
@@ -417,7 +429,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     evs = []
     for i in range(e2e_steps):
-        flush.zero_()
+        flush_and_hold(flush)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         xd.copy_(xh[i % N_WINDOWS], non_blocking=True)
@@ -430,6 +442,10 @@ def run_ours(args, rank, world, local_rank):
     e2e = {"value": e2e_steps * T * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": T * d * 4,
            "d2h_bytes_per_step": T * d * 4}
 
+    workloads = None
+    if not args.no_workloads:
+        workloads = {"zipf": measure_workload("zipf", (8,), dev, flush, stream, peak),
+                     "lowbit": measure_workload("lowbit", (1, 8), dev, flush, stream, peak)}
     stack = None if args.no_stack else measure_stack(args, dev, flush, stream, peak)
     clocks = sampler.stop()
 
@@ -452,7 +468,8 @@ def run_ours(args, rank, world, local_rank):
                        "parallelism": "replicas only" if world > 1 else "1 GPU",
                        "arith": "codes -> exact fp16 integers; mma.sync f16 x (fp16 hi + lo activations), fp32 "
                                 "accumulate; fp32 router, softmax, SwiGLU, combine"},
-            "roofline": roofline, "sweep": sweep, "graph": graph, "stack48": stack, "e2e": e2e, "clocks": clocks,
+            "roofline": roofline, "sweep": sweep, "graph": graph, "workloads": workloads, "stack48": stack, "e2e": e2e,
+            "clocks": clocks,
             "cpu_baseline": cpu,
             "gpu_launches": args.steps,
             "window_us_median": 1e3 * statistics.median(ms), "wall_s_timed_region": wall,
@@ -461,6 +478,51 @@ def run_ours(args, rank, world, local_rank):
         }
         print(json.dumps(line), flush=True)
     win.close()
+
+
+def measure_workload(name, Ts, dev, flush, stream, peak, steps=300):
+    """Another layer shape of the pages' workloads at the given row counts:
+    mean kernel time per window (profiling-mode events around the launch, L2
+    flushed before each window) over its algorithmic bytes."""
+    import numpy as np
+    import torch
+    from slot_decode_window_gb300 import binding, workloads as wlm
+    wl = wlm.WORKLOADS[name]
+    layer = wlm.make_moe_layer(wl.moe, seed=0, cfg_id=wl.cfg_id, device=str(dev))
+    win = binding.Window(layer, max_rows=8)
+    del layer
+    torch.cuda.empty_cache()
+    info = win.info()
+    d = wl.moe.hidden
+    out = {"workload": workload_desc(wl, "|".join(str(t) for t in Ts))}
+    for T in Ts:
+        X = torch.from_numpy(np.stack([wlm.make_window(wl, T, seed=0, window=2000 * T + w) for w in range(16)])).to(dev)
+        Y = torch.empty(T, d, device=dev)
+        nd = []
+        for w in range(16):
+            _, rt = win.forward(X[w], Y, routing=True)
+            nd.append(int(rt["n_distinct"].item()))
+        win.sync()
+        wb = [n * info.expert_bytes + info.shared_bytes + info.router_bytes + 2 * T * d * 4 for n in nd]
+        for i in range(5):
+            win.forward(X[i % 16], Y)
+        win.set_profiling(True)
+        ms, nbytes = [], 0.0
+        for i in range(steps):
+            flush_and_hold(flush)
+            win.forward(X[i % 16], Y)
+            ms.append(win.timings())
+            nbytes += wb[i % 16]
+        win.set_profiling(False)
+        win.sync()
+        tot = sum(ms) / 1e3
+        achieved = nbytes / tot / 1e9
+        out[str(T)] = {"us_per_window_mean": 1e6 * tot / steps, "rows_per_s": steps * T / tot,
+                       "windows_per_s": steps / tot, "algorithmic_MB_per_window": nbytes / steps / 1e6,
+                       "mean_distinct_experts": sum(nd) / len(nd), "achieved_GBps": achieved,
+                       "frac_of_measured_hbm": achieved / peak}
+    win.close()
+    return out
 
 
 def measure_stack(args, dev, flush, stream, peak):
@@ -494,7 +556,7 @@ def measure_stack(args, dev, flush, stream, peak):
     ms = []
     nbytes = 0.0
     for i in range(steps):
-        flush.zero_()
+        flush_and_hold(flush)
         stk.forward(X[i % nw], Y)
         ms.append(stk.timings())
         nbytes += per_window[i % nw]

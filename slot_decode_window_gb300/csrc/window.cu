@@ -504,101 +504,101 @@ __device__ bool grid_barrier(const WindowBufs& W, int* s_ok) {
   return *s_ok != 0;
 }
 
+// Row t (warp t; lane holds experts lane + 32 i): logits as the column-chunk
+// partials summed in chunk order (four chunks' loads in flight at a time, so
+// every CTA gets the same bits), top-k by logit (descending, ties to the lower
+// expert), fp32 softmax over all E, and the selected experts' gate weights.
+__device__ __forceinline__ void plan_row(const LayerDev& L, const WindowBufs& W, SPlan& sp, int t, int lane,
+                                         bool pub) {
+  constexpr int NI = kMaxExperts / 32;
+  const int E = L.E, k = L.k, njb = W.njb;
+  float val[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) val[i] = 0.f;
+  const float* pr = W.partial + (long long)t * E + lane;
+  for (int b0 = 0; b0 < njb; b0 += 4) {
+    float part[4][NI];
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int i = 0; i < NI; ++i)
+        part[b][i] = (b0 + b < njb && lane + 32 * i < E) ? __ldcg(pr + (long long)(b0 + b) * kMaxRows * E + 32 * i)
+                                                          : 0.f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int i = 0; i < NI; ++i) val[i] += part[b][i];
+  }
+  unsigned key[NI];
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E && L.router_b) val[i] += L.router_b[e];
+    if (e < E) finite &= isfinite(val[i]);
+    key[i] = e < E ? ord_f32(val[i]) : 0u;  // 0: below every real logit
+  }
+  if (!__all_sync(0xffffffffu, finite) && lane == 0 && pub) atomicOr(W.err, kErrNonFinite);
+  int esel = 0;
+  float lsel = 0.f, top = 0.f;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    unsigned bk = 0u;
+    int bi_l = 0;
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+      if (key[i] > bk) {
+        bk = key[i];
+        bi_l = i;
+      }
+    const unsigned kmax = __reduce_max_sync(0xffffffffu, bk);
+    const unsigned cand = (bk == kmax && bk != 0u) ? (unsigned)(lane + 32 * bi_l) : 0xffffffffu;
+    int bi = (int)__reduce_min_sync(0xffffffffu, cand);
+    if (bi < 0 || bi >= E) bi = 0;  // only with non-finite logits
+    if ((bi & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < NI; ++i)
+        if (i == (bi >> 5)) key[i] = 0u;
+    }
+    const float lv = unord_f32(kmax);
+    if (j == 0) top = lv;
+    if (lane == j) {
+      esel = bi;
+      lsel = lv;
+    }
+  }
+  // softmax over all E logits, shifted by the largest
+  float z = 0.f;
+#pragma unroll
+  for (int i = 0; i < NI; ++i)
+    if (lane + 32 * i < E) z += expf(val[i] - top);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  const float p = lane < k ? expf(lsel - top) / z : 0.f;
+  float wsum = p;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+  if (lane < k) {
+    const float g = L.renorm ? p / wsum : p;
+    const int ent = t * k + lane;
+    sp.sel[ent] = esel;
+    sp.topk_w[ent] = g;
+    if (pub) {
+      if (W.out_topk_idx) W.out_topk_idx[ent] = esel;
+      if (W.out_topk_w) W.out_topk_w[ent] = g;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // stage P: the routing plan (every CTA, same fixed-order arithmetic)
 // ---------------------------------------------------------------------------
-__device__ __noinline__ void compute_plan(const LayerDev& L, const WindowBufs& W, SPlan& sp, float* lg) {
-  const int T = W.T, E = L.E, k = L.k, njb = W.njb;
+__device__ __noinline__ void compute_plan(const LayerDev& L, const WindowBufs& W, SPlan& sp) {
+  const int T = W.T, E = L.E, k = L.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool pub = blockIdx.x == 0;
-  // 1. logits: the column-chunk partials summed in chunk order; a thread
-  //    issues the loads of up to kU logits before it sums any of them
-  {
-    constexpr int kU = 4, kB = 8;
-    const int n = T * E;
-    for (int i0 = tid; i0 < n; i0 += kU * blockDim.x) {
-      float v[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) v[u] = 0.f;
-      for (int b0 = 0; b0 < njb; b0 += kB) {
-        float part[kU][kB];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int i = i0 + u * blockDim.x;
-#pragma unroll
-          for (int b = 0; b < kB; ++b)
-            part[u][b] = (i < n && b0 + b < njb) ? __ldcg(W.partial + (long long)(b0 + b) * kMaxRows * E + i) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-#pragma unroll
-          for (int b = 0; b < kB; ++b) v[u] += part[u][b];
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = i0 + u * blockDim.x;
-        if (i < n) lg[i] = L.router_b ? v[u] + L.router_b[i % E] : v[u];
-      }
-    }
-  }
-  __syncthreads();
-  STAMP(0, 17);
-  // 2. top-k by logit (descending, ties -> lower expert index) and the fp32
-  //    softmax weights of the chosen experts; warp t owns row t, its logits in
-  //    registers (E <= 256: eight per lane)
-  if (warp < T) {
-    const float* lr = lg + warp * E;
-    unsigned key[kMaxExperts / 32];
-    float val[kMaxExperts / 32];
-    bool finite = true;
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
-      const int e = lane + 32 * i;
-      val[i] = e < E ? lr[e] : 0.f;
-      finite &= isfinite(val[i]);
-      key[i] = e < E ? ord_f32(val[i]) : 0u;  // 0: below every real logit
-    }
-    if (!__all_sync(0xffffffffu, finite) && lane == 0 && pub) atomicOr(W.err, kErrNonFinite);
-    int esel = 0;
-    float lsel = 0.f, top = 0.f;
-    for (int j = 0; j < k; ++j) {
-      unsigned bk = 0u;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i)
-        if (key[i] > bk) { bk = key[i]; be = lane + 32 * i; }
-      const unsigned kmax = __reduce_max_sync(0xffffffffu, bk);
-      int bi = (int)__reduce_min_sync(0xffffffffu, (bk == kmax && be != 0x7fffffff) ? (unsigned)be : 0xffffffffu);
-      if (bi < 0 || bi >= E) bi = 0;  // only with non-finite logits
-#pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i)
-        if (lane + 32 * i == bi) key[i] = 0u;
-      const float lv = unord_f32(kmax);
-      if (j == 0) top = lv;
-      if (lane == j) { esel = bi; lsel = lv; }
-    }
-    // softmax over all E logits, shifted by the largest
-    float z = 0.f;
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i)
-      if (lane + 32 * i < E) z += expf(val[i] - top);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    const float p = lane < k ? expf(lsel - top) / z : 0.f;
-    float wsum = p;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-    if (lane < k) {
-      const float g = L.renorm ? p / wsum : p;
-      const int ent = warp * k + lane;
-      sp.sel[ent] = esel;
-      sp.topk_w[ent] = g;
-      if (pub) {
-        if (W.out_topk_idx) W.out_topk_idx[ent] = esel;
-        if (W.out_topk_w) W.out_topk_w[ent] = g;
-      }
-    }
-  }
+  // 1-2. row t (warp t): logits, top-k, softmax, gate weights
+  if (warp < T) plan_row(L, W, sp, warp, lane, pub);
   __syncthreads();
   STAMP(0, 18);
   // 3. grouping: entries ordered by expert, then by entry index.  Warps 0 and 1
@@ -1365,7 +1365,7 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
                                           const Ring& rg, const Smem& m, RingPos& rp, int& buf) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // P: the routing plan (the ring is free until the producer starts: logits scratch)
-  compute_plan(L, W, sp, reinterpret_cast<float*>(m.ring));
+  compute_plan(L, W, sp);
   STAMP(0, 3);
   const int nd = sp.nd;
   if (nd < 0 || nd > L.E) {
