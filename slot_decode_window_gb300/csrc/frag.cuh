@@ -29,9 +29,7 @@ __host__ __device__ inline void frag_main_pos<2>(int i, int& off, float& factor)
   // and the odd block of a pair carries factors 16 and 64.
   const int blk = i >> 4, e = i & 15, c = e >> 2, u = e & 3;
   const int ks = blk >> 3, bi = blk & 7;
-  const float f_even[2] = {1.0f, 0.25f};
-  const float f_odd[2] = {1.0f / 16.0f, 1.0f / 64.0f};
-  factor = (bi & 1) ? f_odd[u >> 1] : f_even[u >> 1];
+  factor = (bi & 1) ? ((u >> 1) ? 1.0f / 64.0f : 1.0f / 16.0f) : ((u >> 1) ? 0.25f : 1.0f);
   off = ((ks * 4 + c) * 32) + bi * 4 + u;
 }
 
