@@ -143,6 +143,7 @@ struct KernelCfg {
   int bsum_halves;         // B sums halves per set: nmk_max*8*4*4
   int nsets;               // 1 (rows <= 4) or 2
   int total_bytes;
+  int direct;              // window kernel on the register-fed path (no producer, no ring)
   PhaseCfg ph[4];
 };
 

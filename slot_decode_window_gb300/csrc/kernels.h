@@ -8,9 +8,11 @@ constexpr int kRouterCols = 512;  // columns per router partial-logit chunk
 
 // Shared-memory plan of the window kernel for one layer shape.
 KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit);
-cudaError_t window_set_attrs(int bits, int smem_bytes);
+// The same with the register-fed path when the shape allows it (C.direct).
+KernelCfg window_cfg_direct(const LayerDev& L, int max_rows, int smem_limit);
+cudaError_t window_set_attrs(int bits, int direct, int smem_bytes);
 // CTAs of the window kernel that one SM holds (0 if it does not fit).
-int window_blocks_per_sm(int bits, int smem_bytes);
+int window_blocks_per_sm(int bits, int direct, int smem_bytes);
 // One window: router, grouping, gate/up, down and combine in one cooperative launch.
 cudaError_t launch_window(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, int grid, cudaStream_t s);
 

@@ -211,18 +211,18 @@ strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe
   W.sbuf = reinterpret_cast<float*>(wsb + o_sb);
 
   const int limit = optin - 12288;  // leave room for the kernel's static shared memory
-  h->cfg = window_cfg(L, desc->max_rows, limit);
-  if (h->cfg.nstages < 2) {
+  h->cfg = window_cfg_direct(L, desc->max_rows, limit);
+  if (!h->cfg.direct && h->cfg.nstages < 2) {
     free_handle(h);
     return STRATA_EUNSUPPORTED;
   }
-  if (window_set_attrs(bits, h->cfg.total_bytes) != cudaSuccess) {
+  if (window_set_attrs(bits, h->cfg.direct, h->cfg.total_bytes) != cudaSuccess) {
     cudaGetLastError();
     free_handle(h);
     return STRATA_ECUDA;
   }
   // the window kernel's CTAs wait on one another: all of them must be resident
-  if (window_blocks_per_sm(bits, h->cfg.total_bytes) < 1) {
+  if (window_blocks_per_sm(bits, h->cfg.direct, h->cfg.total_bytes) < 1) {
     free_handle(h);
     return STRATA_EUNSUPPORTED;
   }

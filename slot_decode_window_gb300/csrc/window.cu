@@ -36,6 +36,8 @@
 // to the fp32 accumulator fragment, and adds the min term with one more MMA
 // against per-block activation sums.  Lanes whose activation columns are
 // unused (groups of fewer than 4 or 8 rows) skip their operand loads.
+#include <cstdlib>
+
 #include "common.cuh"
 #include "frag.cuh"
 #include "kernels.h"
@@ -135,10 +137,35 @@ __device__ __forceinline__ int bmain_off(int ks, int p, int col, int c) {
 // bk points at this lane's slot of plane 0 of the k-step (set 0); lanes whose
 // MMA column is unused point at column 0 instead (same-address reads
 // broadcast, and a column of the product depends only on that column of B).
-template <int BITS, bool PAIRED>
-__device__ __forceinline__ void kstep_mma(const uint8_t* __restrict__ ch, const __half* __restrict__ bk, int bm_set,
-                                          int lane, float (&acc)[4]) {
+// One k-step's A-side words of one lane: its 16 code bytes and the scale
+// record(s) of its rows g and g + 8 (4-bit: 8 bytes; 2-bit: 32 bytes).
+template <int BITS> struct KWords;
+template <> struct KWords<4> {
+  uint4 cw;
+  uint2 sr;
+};
+template <> struct KWords<2> {
+  uint4 cw;
+  uint4 sa, sb;
+};
+
+template <int BITS>
+__device__ __forceinline__ KWords<BITS> kwords_smem(const uint8_t* __restrict__ ch, int lane) {
   const int g = lane >> 2;
+  KWords<BITS> kw;
+  kw.cw = *reinterpret_cast<const uint4*>(ch + lane * 16);
+  if constexpr (BITS == 4) {
+    kw.sr = *reinterpret_cast<const uint2*>(ch + 512 + g * 8);
+  } else {
+    kw.sa = *reinterpret_cast<const uint4*>(ch + 512 + g * 32);       // s(g, b0..b7)
+    kw.sb = *reinterpret_cast<const uint4*>(ch + 512 + g * 32 + 16);  // s(g+8, b0..b7)
+  }
+  return kw;
+}
+
+template <int BITS, bool PAIRED>
+__device__ __forceinline__ void kstep_compute(const KWords<BITS>& kw, const __half* __restrict__ bk, int bm_set,
+                                              int lane, float (&acc)[4]) {
   const float z4[4] = {0.f, 0.f, 0.f, 0.f};
   if constexpr (BITS == 4) {
     const uint4 bA = *reinterpret_cast<const uint4*>(bk);
@@ -148,8 +175,8 @@ __device__ __forceinline__ void kstep_mma(const uint8_t* __restrict__ ch, const 
       lA = *reinterpret_cast<const uint4*>(bk + bm_set);
       lB = *reinterpret_cast<const uint4*>(bk + bm_set + 256);
     }
-    const uint4 cw = *reinterpret_cast<const uint4*>(ch + lane * 16);
-    const uint2 sr = *reinterpret_cast<const uint2*>(ch + 512 + g * 8);
+    const uint4 cw = kw.cw;
+    const uint2 sr = kw.sr;
     const float2 sg = __half22float2(*reinterpret_cast<const __half2*>(&sr.x));
     const float2 s8 = __half22float2(*reinterpret_cast<const __half2*>(&sr.y));
 #pragma unroll
@@ -176,9 +203,7 @@ __device__ __forceinline__ void kstep_mma(const uint8_t* __restrict__ ch, const 
       acc[3] = fmaf(s8v, d[3], acc[3]);
     }
   } else {
-    const uint4 cw = *reinterpret_cast<const uint4*>(ch + lane * 16);
-    const uint4 sa = *reinterpret_cast<const uint4*>(ch + 512 + g * 32);       // s(g, b0..b7)
-    const uint4 sb = *reinterpret_cast<const uint4*>(ch + 512 + g * 32 + 16);  // s(g+8, b0..b7)
+    const uint4 cw = kw.cw, sa = kw.sa, sb = kw.sb;
     const uint32_t cwv[4] = {cw.x, cw.y, cw.z, cw.w};
     const uint32_t sav[4] = {sa.x, sa.y, sa.z, sa.w};
     const uint32_t sbv[4] = {sb.x, sb.y, sb.z, sb.w};
@@ -211,6 +236,13 @@ __device__ __forceinline__ void kstep_mma(const uint8_t* __restrict__ ch, const 
       acc[3] = fmaf(s8p.y, d[3], acc[3]);
     }
   }
+}
+
+// One k-step of one sub-tile from a staged chunk in shared memory.
+template <int BITS, bool PAIRED>
+__device__ __forceinline__ void kstep_mma(const uint8_t* __restrict__ ch, const __half* __restrict__ bk, int bm_set,
+                                          int lane, float (&acc)[4]) {
+  kstep_compute<BITS, PAIRED>(kwords_smem<BITS>(ch, lane), bk, bm_set, lane, acc);
 }
 
 // This warp's share of one staged chunk of its sub-tile: k-steps [k0, k1)
@@ -272,6 +304,7 @@ struct SPlan {
   int wscan[32];
   int wcnt[2][kMaxExperts];         // per-warp expert counts of the grouping pass
   int finish[kMaxEntries * 4];      // row slices this CTA combines
+  int fifo_tag[kConsumerWarps][8];  // warp-streamed path: the items in each warp's FIFO slots
   int nfinish;
   int ok;                           // the grid barrier passed
   PhaseTasks pt[4];                 // gate/up, down, dense q/k/v, dense o
@@ -1039,67 +1072,156 @@ __device__ __forceinline__ float frag_pick(const float4 a, int idx, bool paired)
   return paired ? lo + hi : ((idx & 1) ? hi : lo);
 }
 
+// Group state of the consumer loop: rows of the current group and their MMA
+// column layout (paired: 8 columns = 4 rows x (hi, lo); else two column sets).
+struct GroupState {
+  int cur = -2;
+  int R = 0, ent_off = 0;
+  bool paired = true, bon = true;
+  int lane_b = 0;
+  uint32_t inv_d = 0;  // ceil(2^16 / (16 R)): i / (16 R) == (i * inv_d) >> 16 for i < 512
+};
+
+// Enter task tk's group (all consumer threads): its rows, the bounded wait for
+// its gate/up tasks (phase 1), and its activations staged in B.
+template <int BITS, int PHASE>
+__device__ __forceinline__ void enter_group(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, SPlan& sp,
+                                            const Task& tk, int K, volatile int* abort_flag, __half* bm, __half* bs,
+                                            GroupState& gs) {
+  const int tid = threadIdx.x, lane = tid & 31, g = lane >> 2;
+  if (tk.shared) {
+    gs.R = W.T;
+    gs.ent_off = 0;
+  } else {
+    gs.R = sp.counts[tk.expert];
+    gs.ent_off = sp.offsets[tk.expert];
+  }
+  if (gs.R < 1 || gs.R > kMaxRows) {
+    atomicOr(W.err, kErrIndex);
+    gs.R = gs.R < 1 ? 1 : kMaxRows;
+  }
+  const int R = gs.R;
+  gs.paired = R <= 4;
+  gs.bon = gs.paired ? (g < 2 * R) : (g < R);
+  gs.lane_b = gs.bon ? lane : (lane & 3);
+  gs.inv_d = (65536u + 16u * R - 1u) / (16u * R);
+  if (PHASE == 1) {
+    // wait (bounded) until every gate/up task of this group has landed
+    if (tid == 0) {
+      const int need = tk.shared ? sp.pt[0].ntask_s : sp.pt[0].ntask_e;
+      const long long t0 = clock64();
+      while (!*abort_flag && ld_acquire(W.done_gu + tk.group) < need) {
+        if (clock64() - t0 > kWaitCycles) {
+          atomicOr(W.err, kErrTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    consumer_sync();
+    if (gs.cur == -2) STAMP(0, 6);
+  }
+  // the previous task's barrier guarantees no warp still reads the old fragments
+  load_group_B<BITS, PHASE>(L, W, sp, C, bm, bs, tk.shared, R, gs.ent_off, PHASE == 3 ? L.dkv : K, tid);
+  consumer_sync();
+  if (PHASE == 1 && gs.cur == -2) STAMP(0, 7);
+  gs.cur = tk.group;
+}
+
+// One task's epilogue: the cross-warp sums of its partials (rb) in a fixed
+// order, on consecutive threads of one or two warps rotating with the task.
+template <int BITS, int PHASE, int NS>
+__device__ __forceinline__ void task_epilogue(const LayerDev& L, const WindowBufs& W, const SPlan& sp,
+                                              const float4* rb, const Task& tk, int task, const GroupState& gs) {
+  constexpr int kMT = PHASE == 0 ? NS / 2 : NS;
+  constexpr int kWPS = kConsumerWarps / NS;
+  const int tid = threadIdx.x, lane = tid & 31;
+  // ---------------- epilogue: cross-warp sums in a fixed order ----------------
+  // outputs on consecutive threads of one or two warps, rotating with the task,
+  // so the other warps go straight on to the next task
+  const int eo = (tid + 32 * (task & (kConsumerWarps - 1))) & (kConsumerThreads - 1);
+  if (PHASE == 0) {
+    for (int i = eo; i < kMT * 16 * gs.R; i += kConsumerThreads) {
+      const int m = (int)(((uint32_t)i * gs.inv_d) >> 16), rem = i - m * 16 * gs.R;
+      const int r = rem >> 4, row = rem & 15;
+      const int src_lane = (row & 7) * 4 + (gs.paired ? r : (r >> 1));
+      const int idx = ((row >> 3) << 1) + (gs.paired ? 0 : (r & 1));
+      float gv = 0.f, uv = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWPS; ++w) {
+        gv += frag_pick(rb[(m * kWPS + w) * 32 + src_lane], idx, gs.paired);
+        uv += frag_pick(rb[((kMT + m) * kWPS + w) * 32 + src_lane], idx, gs.paired);
+      }
+      // h = silu(gate) * up, stored as the down phase's activation fragments:
+      // fp16 hi/lo parts at the element's fragment slot, and the sum of the 16
+      // elements of this sub-tile (held by 16 consecutive lanes: i % 16 == row)
+      const int f = (tk.tile + m) * 16 + row;
+      const float h = silu_f32(gv) * uv;
+      const int Kh = tk.shared ? L.Fs : L.F;
+      const long long hrow = tk.shared ? r : sp.entries[gs.ent_off + r];
+      __half* hb = (tk.shared ? W.shfrag : W.hfrag) + hrow * 2 * Kh;
+      int off;
+      float fac;
+      frag_main_pos<BITS>(f, off, fac);
+      __half hi, lo;
+      split_hi_lo(h * fac, hi, lo);
+      hb[off] = hi;
+      hb[Kh + off] = lo;
+      const unsigned half_mask = 0xffffu << (lane & 16);
+      float ps = h;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) ps += __shfl_xor_sync(half_mask, ps, o);
+      if (row == 0) (tk.shared ? W.shsum : W.hsum)[hrow * (Kh / 16) + f / 16] = ps;
+    }
+  } else {
+    for (int i = eo; i < NS * 16 * gs.R; i += kConsumerThreads) {
+      const int s = (int)(((uint32_t)i * gs.inv_d) >> 16), rem = i - s * 16 * gs.R;
+      const int r = rem >> 4, row = rem & 15;
+      const int src_lane = (row & 7) * 4 + (gs.paired ? r : (r >> 1));
+      const int idx = ((row >> 3) << 1) + (gs.paired ? 0 : (r & 1));
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWPS; ++w) v += frag_pick(rb[(s * kWPS + w) * 32 + src_lane], idx, gs.paired);
+      const int drow = (tk.tile + s) * 16 + row;
+      if constexpr (PHASE == 2) {
+        // rows of [Wq; Wk; Wv]
+        if (drow < L.dq) {
+          if (W.q_out) W.q_out[(long long)r * L.dq + drow] = v;
+        } else if (drow < L.dq + L.dkv) {
+          if (W.k_out) W.k_out[(long long)r * L.dkv + drow - L.dq] = v;
+        } else {
+          W.v[(long long)r * L.dkv + drow - L.dq - L.dkv] = v;
+        }
+      } else if constexpr (PHASE == 3) {
+        W.x1[(long long)r * L.d + drow] = W.x[(long long)r * L.d + drow] + v;
+      } else if (tk.shared) {
+        W.sbuf[(long long)r * L.d + drow] = v;
+      } else {
+        const int ent = sp.entries[gs.ent_off + r];
+        W.obuf[(long long)ent * L.d + drow] = sp.topk_w[ent] * v;
+      }
+    }
+  }
+}
+
 template <int BITS, int PHASE, int NS>
 __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, SPlan& sp, const Ring& rg,
                         __half* bm, __half* bs, float4* red, RingPos& rp, int& buf) {
-  constexpr int kMT = PHASE == 0 ? NS / 2 : NS;  // row tiles per task
-  constexpr int kWPS = kConsumerWarps / NS;      // warps per sub-tile
+  constexpr int kWPS = kConsumerWarps / NS;  // warps per sub-tile
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PhaseCfg& P = C.ph[PHASE];
   const PhaseTasks& pt = sp.pt[PHASE];
   const bool has_shared = L.Fs > 0;
   const int sub = warp / kWPS, kg = warp % kWPS;
-  const int g = lane >> 2;
-  int cur = -2;
-  int R = 0, ent_off = 0;
-  bool paired = true, bon = true;
-  int lane_b = lane;
-  uint32_t inv_d = 0;  // ceil(2^16 / (16 R)): i / (16 R) == (i * inv_d) >> 16 for i < 512
+  GroupState gs;
   TaskWalk tw;
   if (pt.t0 < pt.t1) tw.start(pt.t0, pt, has_shared, sp);
   for (int task = pt.t0; task < pt.t1; ++task, tw.next(pt, has_shared, sp)) {
     const Task& tk = tw.tk;
     if (!tk.shared && (unsigned)tk.expert >= (unsigned)L.E) break;  // flagged by the producer
     const int K = PHASE == 0 ? L.d : PHASE == 1 ? (tk.shared ? L.Fs : L.F) : PHASE == 2 ? L.d : L.dq;
-    if (tk.group != cur) {
-      if (tk.shared) {
-        R = W.T;
-        ent_off = 0;
-      } else {
-        R = sp.counts[tk.expert];
-        ent_off = sp.offsets[tk.expert];
-      }
-      if (R < 1 || R > kMaxRows) {
-        atomicOr(W.err, kErrIndex);
-        R = R < 1 ? 1 : kMaxRows;
-      }
-      paired = R <= 4;
-      bon = paired ? (g < 2 * R) : (g < R);
-      lane_b = bon ? lane : (lane & 3);
-      inv_d = (65536u + 16u * R - 1u) / (16u * R);
-      if (PHASE == 1) {
-        // wait (bounded) until every gate/up task of this group has landed
-        if (tid == 0) {
-          const int need = tk.shared ? sp.pt[0].ntask_s : sp.pt[0].ntask_e;
-          const long long t0 = clock64();
-          while (!*rg.abort_flag && ld_acquire(W.done_gu + tk.group) < need) {
-            if (clock64() - t0 > kWaitCycles) {
-              atomicOr(W.err, kErrTimeout);
-              *rg.abort_flag = 1;
-              break;
-            }
-            __nanosleep(32);
-          }
-        }
-        consumer_sync();
-        if (cur == -2) STAMP(0, 6);
-      }
-      // the previous task's barrier guarantees no warp still reads the old fragments
-      load_group_B<BITS, PHASE>(L, W, sp, C, bm, bs, tk.shared, R, ent_off, PHASE == 3 ? L.dkv : K, tid);
-      consumer_sync();
-      if (PHASE == 1 && cur == -2) STAMP(0, 7);
-      cur = tk.group;
-    }
+    if (tk.group != gs.cur) enter_group<BITS, PHASE>(L, W, C, sp, tk, K, rg.abort_flag, bm, bs, gs);
     const int kv = (PHASE == 1 && tk.shared) ? 1 : 0;
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
     if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 0);
@@ -1114,12 +1236,12 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
         if (PHASE < 2 && ch == 0) TRACE(0, PHASE, task - pt.t0, 1);
         const uint8_t* st = rg.base + (size_t)stage * C.stage_bytes + sub * P.sub_stride;
         constexpr bool kVmap = PHASE == 3;
-        if (paired)
+        if (gs.paired)
           chunk_mma<BITS, true, kVmap>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
-                                       C.bsum_halves, lane_b, lane, acc, accm, L.kph_log2, L.kpg_log2);
+                                       C.bsum_halves, gs.lane_b, lane, acc, accm, L.kph_log2, L.kpg_log2);
         else
           chunk_mma<BITS, false, kVmap>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
-                                        C.bsum_halves, lane_b, lane, acc, accm, L.kph_log2, L.kpg_log2);
+                                        C.bsum_halves, gs.lane_b, lane, acc, accm, L.kph_log2, L.kpg_log2);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&rg.empty[stage]);
@@ -1132,73 +1254,191 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
     consumer_sync();
     if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 3);
 
-    // ---------------- epilogue: cross-warp sums in a fixed order ----------------
-    // outputs on consecutive threads of one or two warps, rotating with the task,
-    // so the other warps go straight on to the next task
-    const int eo = (tid + 32 * (task & (kConsumerWarps - 1))) & (kConsumerThreads - 1);
-    if (PHASE == 0) {
-      for (int i = eo; i < kMT * 16 * R; i += kConsumerThreads) {
-        const int m = (int)(((uint32_t)i * inv_d) >> 16), rem = i - m * 16 * R;
-        const int r = rem >> 4, row = rem & 15;
-        const int src_lane = (row & 7) * 4 + (paired ? r : (r >> 1));
-        const int idx = ((row >> 3) << 1) + (paired ? 0 : (r & 1));
-        float gv = 0.f, uv = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWPS; ++w) {
-          gv += frag_pick(rb[(m * kWPS + w) * 32 + src_lane], idx, paired);
-          uv += frag_pick(rb[((kMT + m) * kWPS + w) * 32 + src_lane], idx, paired);
-        }
-        // h = silu(gate) * up, stored as the down phase's activation fragments:
-        // fp16 hi/lo parts at the element's fragment slot, and the sum of the 16
-        // elements of this sub-tile (held by 16 consecutive lanes: i % 16 == row)
-        const int f = (tk.tile + m) * 16 + row;
-        const float h = silu_f32(gv) * uv;
-        const int Kh = tk.shared ? L.Fs : L.F;
-        const long long hrow = tk.shared ? r : sp.entries[ent_off + r];
-        __half* hb = (tk.shared ? W.shfrag : W.hfrag) + hrow * 2 * Kh;
-        int off;
-        float fac;
-        frag_main_pos<BITS>(f, off, fac);
-        __half hi, lo;
-        split_hi_lo(h * fac, hi, lo);
-        hb[off] = hi;
-        hb[Kh + off] = lo;
-        const unsigned half_mask = 0xffffu << (lane & 16);
-        float ps = h;
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) ps += __shfl_xor_sync(half_mask, ps, o);
-        if (row == 0) (tk.shared ? W.shsum : W.hsum)[hrow * (Kh / 16) + f / 16] = ps;
-      }
+    task_epilogue<BITS, PHASE, NS>(L, W, sp, rb, tk, task, gs);
+    buf ^= 1;
+  }
+  if (PHASE == 0) {
+    // publish this CTA's finished gate/up tasks: one fence, then per-group counts
+    __threadfence();
+    consumer_sync();
+    for (int task = pt.t0 + tid; task < pt.t1; task += kConsumerThreads) {
+      const Task tk = decode_task(task, pt, has_shared, sp);
+      atomicAdd(W.done_gu + tk.group, 1);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// warp-streamed consumers (the window kernel): every warp copies its own share
+// of each task into a private FIFO of shared-memory slots with 16-byte
+// cp.async, kDepth items ahead; no producer warp and no CTA-wide stage ring
+// ---------------------------------------------------------------------------
+enum : int { kItemK = 1, kItemM = 2, kItemFirst = 4, kItemLast = 8 };
+
+// FIFO depth in items (the path is used for 2-bit layers)
+template <int BITS> struct FifoDepth { static constexpr int value = 4; };
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// A warp's item stream over its CTA's task range of one phase: in each task
+// the warp takes k-steps [k0, k1) and min groups [m0, m1) of sub-tile `sub`
+// (k-steps first).  An item is one k-step chunk (512 code bytes and the scale
+// records, laid out as in the tile) or one 512-byte min fragment.  Every
+// warp has at least one item in every task (the kernel is used only when each
+// warp's k-range is non-empty).
+template <int BITS, int PHASE, int NS>
+struct DStream {
+  static constexpr int kMT = PHASE == 0 ? NS / 2 : NS;
+  static constexpr int kWPS = kConsumerWarps / NS;
+  TaskWalk tw;
+  int task, t1, i, n, nk, k0, m0, nks;
+  const uint8_t* tile;
+
+  __device__ __forceinline__ void set(const LayerDev& L, int sub, int kg, volatile int* abort_flag, unsigned* err) {
+    const Task& tk = tw.tk;
+    if (!tk.shared && (unsigned)tk.expert >= (unsigned)L.E) {  // only with a corrupt plan
+      atomicOr(err, kErrIndex);
+      *abort_flag = 1;
+      task = t1;
+      return;
+    }
+    const int K = PHASE == 0 ? L.d : (tk.shared ? L.Fs : L.F);
+    nks = K / Fmt<BITS>::kKstep;
+    const int nmk = (K / Fmt<BITS>::kBlock + 15) / 16;
+    k0 = kg * nks / kWPS;
+    const int k1 = (kg + 1) * nks / kWPS;
+    m0 = kg * nmk / kWPS;
+    const int m1 = (kg + 1) * nmk / kWPS;
+    nk = k1 - k0;
+    n = nk + (m1 - m0);
+    const int tbytes = nks * Fmt<BITS>::kChunk + nmk * 512;
+    const MatRef M = task_mat<PHASE, kMT>(L, tk.shared, sub);
+    const int t = tk.tile + (PHASE == 0 && sub >= kMT ? sub - kMT : sub);
+    tile = M.base + (tk.shared ? 0LL : (long long)tk.expert * M.mat_bytes) + (long long)t * tbytes;
+    i = 0;
+  }
+  __device__ __forceinline__ void start(const LayerDev& L, const SPlan& sp, const PhaseTasks& pt, int sub, int kg,
+                                        volatile int* abort_flag, unsigned* err) {
+    task = pt.t0;
+    t1 = pt.t1;
+    if (task < t1) {
+      tw.start(task, pt, L.Fs > 0, sp);
+      set(L, sub, kg, abort_flag, err);
+    }
+  }
+  // copy the next item into `dst` (this warp's slot; not waited for) and
+  // return its tag: bit 0 k-step, bit 1 min group, bit 2 first item of its
+  // task, bit 3 last item, bits 4.. the k-step or min-group index; 0 = none
+  __device__ __forceinline__ int issue(uint8_t* dst, const LayerDev& L, const SPlan& sp, const PhaseTasks& pt,
+                                       int sub, int kg, int lane, volatile int* abort_flag, unsigned* err) {
+    if (task >= t1) return 0;
+    int tag = (i == 0 ? kItemFirst : 0) | (i == n - 1 ? kItemLast : 0);
+    if (i < nk) {
+      constexpr int kScaleBytes = Fmt<BITS>::kChunk - 512;
+      const int ks = k0 + i;
+      const uint8_t* p = tile + (size_t)ks * Fmt<BITS>::kChunk;
+      cp_async16(dst + lane * 16, p + lane * 16);
+      if (lane * 16 < kScaleBytes) cp_async16(dst + 512 + lane * 16, p + 512 + lane * 16);
+      tag |= kItemK | (ks << 4);
     } else {
-      for (int i = eo; i < NS * 16 * R; i += kConsumerThreads) {
-        const int s = (int)(((uint32_t)i * inv_d) >> 16), rem = i - s * 16 * R;
-        const int r = rem >> 4, row = rem & 15;
-        const int src_lane = (row & 7) * 4 + (paired ? r : (r >> 1));
-        const int idx = ((row >> 3) << 1) + (paired ? 0 : (r & 1));
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWPS; ++w) v += frag_pick(rb[(s * kWPS + w) * 32 + src_lane], idx, paired);
-        const int drow = (tk.tile + s) * 16 + row;
-        if constexpr (PHASE == 2) {
-          // rows of [Wq; Wk; Wv]
-          if (drow < L.dq) {
-            if (W.q_out) W.q_out[(long long)r * L.dq + drow] = v;
-          } else if (drow < L.dq + L.dkv) {
-            if (W.k_out) W.k_out[(long long)r * L.dkv + drow - L.dq] = v;
-          } else {
-            W.v[(long long)r * L.dkv + drow - L.dq - L.dkv] = v;
-          }
-        } else if constexpr (PHASE == 3) {
-          W.x1[(long long)r * L.d + drow] = W.x[(long long)r * L.d + drow] + v;
-        } else if (tk.shared) {
-          W.sbuf[(long long)r * L.d + drow] = v;
-        } else {
-          const int ent = sp.entries[ent_off + r];
-          W.obuf[(long long)ent * L.d + drow] = sp.topk_w[ent] * v;
-        }
+      const int mk = m0 + (i - nk);
+      cp_async16(dst + lane * 16, tile + (size_t)nks * Fmt<BITS>::kChunk + mk * 512 + lane * 16);
+      tag |= kItemM | (mk << 4);
+    }
+    if (++i == n) {
+      if (++task < t1) {
+        tw.next(pt, L.Fs > 0, sp);
+        set(L, sub, kg, abort_flag, err);
       }
     }
-    buf ^= 1;
+    return tag;
+  }
+};
+
+// One phase's tasks on the warp-streamed path (all 16 warps).  Warp w keeps
+// kDepth items of its stream in flight in its FIFO slots (one cp.async group
+// per item); items are consumed in order, across task and group boundaries,
+// so a phase's first copies are in flight while its first group's
+// activations are staged.
+template <int BITS, int PHASE, int NS>
+__device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, SPlan& sp,
+                               volatile int* abort_flag, __half* bm, __half* bs, float4* red, uint8_t* fifo,
+                               int& buf) {
+  constexpr int kWPS = kConsumerWarps / NS;
+  constexpr int kDepth = FifoDepth<BITS>::value;
+  constexpr int kSlot = Fmt<BITS>::kChunk;
+  constexpr int S = Fmt<BITS>::kBHalves;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const PhaseTasks& pt = sp.pt[PHASE];
+  const bool has_shared = L.Fs > 0;
+  const int sub = warp / kWPS, kg = warp % kWPS;
+  if (pt.t0 < pt.t1) {
+    uint8_t* slots = fifo + (size_t)warp * kDepth * kSlot;
+    int* tags = sp.fifo_tag[warp];
+    DStream<BITS, PHASE, NS> ds;
+    ds.start(L, sp, pt, sub, kg, abort_flag, W.err);
+#pragma unroll
+    for (int q = 0; q < kDepth; ++q) {
+      const int tg = ds.issue(slots + q * kSlot, L, sp, pt, sub, kg, lane, abort_flag, W.err);
+      if (lane == 0) tags[q] = tg;
+      cp_async_commit();
+    }
+    GroupState gs;
+    TaskWalk tw;
+    tw.start(pt.t0, pt, has_shared, sp);
+    int task = pt.t0, slot = 0;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
+    while (true) {
+      cp_async_wait_group<kDepth - 1>();  // this lane's copies of the oldest item have landed
+      __syncwarp();
+      const int tag = tags[slot];
+      if (tag == 0) break;
+      const uint8_t* it = slots + slot * kSlot;
+      const Task& tk = tw.tk;
+      if (tag & kItemFirst) {
+        const int K = PHASE == 0 ? L.d : (tk.shared ? L.Fs : L.F);
+        if (tk.group != gs.cur) enter_group<BITS, PHASE>(L, W, C, sp, tk, K, abort_flag, bm, bs, gs);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = accm[q] = 0.f;
+      }
+      if (!*abort_flag) {
+        const int idx = tag >> 4;
+        if (tag & kItemK) {
+          const __half* bk = bm + idx * 32 * S + gs.lane_b * 8;
+          if (gs.paired) kstep_mma<BITS, true>(it, bk, C.bmain_halves, lane, acc);
+          else kstep_mma<BITS, false>(it, bk, C.bmain_halves, lane, acc);
+        } else {
+          const uint4 am = *reinterpret_cast<const uint4*>(it + lane * 16);
+          const uint2 b = *reinterpret_cast<const uint2*>(bs + idx * 128 + gs.lane_b * 4);
+          mma16816(accm, am.x, am.y, am.z, am.w, b.x, b.y, accm);
+          if (!gs.paired) {
+            const uint2 l = *reinterpret_cast<const uint2*>(bs + C.bsum_halves + idx * 128 + gs.lane_b * 4);
+            mma16816(accm, am.x, am.y, am.z, am.w, l.x, l.y, accm);
+          }
+        }
+      }
+      __syncwarp();  // every lane is done with the slot before it is refilled
+      {
+        const int tg = ds.issue(slots + slot * kSlot, L, sp, pt, sub, kg, lane, abort_flag, W.err);
+        if (lane == 0) tags[slot] = tg;
+        cp_async_commit();
+      }
+      slot = slot + 1 == kDepth ? 0 : slot + 1;
+      if (tag & kItemLast) {
+        float4* rb = red + buf * (kConsumerWarps * 32);
+        rb[warp * 32 + lane] = make_float4(fmaf(acc[0], kDqUnscale, accm[0]), fmaf(acc[1], kDqUnscale, accm[1]),
+                                           fmaf(acc[2], kDqUnscale, accm[2]), fmaf(acc[3], kDqUnscale, accm[3]));
+        consumer_sync();
+        task_epilogue<BITS, PHASE, NS>(L, W, sp, rb, tk, task, gs);
+        buf ^= 1;
+        if (++task == pt.t1) break;
+        tw.next(pt, has_shared, sp);
+      }
+    }
+    cp_async_wait_all();  // nothing of this phase may land in the FIFO later
+    __syncwarp();
   }
   if (PHASE == 0) {
     // publish this CTA's finished gate/up tasks: one fence, then per-group counts
@@ -1360,7 +1600,7 @@ __device__ __forceinline__ void init_cta(const KernelCfg& C, const Smem& m, vola
 // combine (larger windows combine after a grid barrier, in the caller).
 // Returns false when the plan is unusable (the error word says why); every
 // CTA sees the same plan, so all return alike.
-template <int BITS>
+template <int BITS, bool DIRECT = false>
 __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, SPlan& sp,
                                           const Ring& rg, const Smem& m, RingPos& rp, int& buf) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1390,7 +1630,9 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
     const int tiles_g = L.d / 16;
     const long long all1 = (long long)((has_shared ? 1 : 0) + nd) * tiles_g;
     int mt = C.ph[1].max_sub;
-    while (mt > 1 && (tiles_g % mt != 0 || all1 / mt < (long long)gridDim.x)) mt >>= 1;
+    // (the register-fed path keeps >= 2 tiles per task: every warp then has
+    // at least one k-step of each task)
+    while (mt > (DIRECT ? 2 : 1) && (tiles_g % mt != 0 || all1 / mt < (long long)gridDim.x)) mt >>= 1;
     p1.mt = mt;
     p1.ntask_s = has_shared ? tiles_g / mt : 0;
     p1.ntask_e = tiles_g / mt;
@@ -1407,6 +1649,19 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
   STAMP(0, 4);
 
   const int ns0 = 2 * sp.pt[0].mt, ns1 = sp.pt[1].mt;
+  if constexpr (DIRECT) {
+    if (ns0 == 4) consume_direct<BITS, 0, 4>(L, W, C, sp, rg.abort_flag, m.bm, m.bs, m.red, m.ring, buf);
+    else consume_direct<BITS, 0, 2>(L, W, C, sp, rg.abort_flag, m.bm, m.bs, m.red, m.ring, buf);
+    const bool slices = W.T < kGridCombineRows;  // else the caller combines after a grid barrier
+    if (ns1 == 4) {
+      consume_direct<BITS, 1, 4>(L, W, C, sp, rg.abort_flag, m.bm, m.bs, m.red, m.ring, buf);
+      if (slices) combine<4>(L, W, sp);
+    } else {
+      consume_direct<BITS, 1, 2>(L, W, C, sp, rg.abort_flag, m.bm, m.bs, m.red, m.ring, buf);
+      if (slices) combine<2>(L, W, sp);
+    }
+    return true;
+  }
   if (warp == kConsumerWarps) {
     // ---------------- producer ----------------
     if (lane == 0) {
@@ -1509,6 +1764,28 @@ __global__ void __launch_bounds__(kExpertThreads, 1) window_kernel(LayerDev L, W
     STAMP(0, 10);
     combine_all(L, W);
     STAMP(0, 16);
+  }
+}
+
+// The window kernel on the register-fed path: 16 warps, no producer warp and
+// no stage ring (the ring's place holds only stage R's staged rows of x).
+template <int BITS>
+__global__ void __launch_bounds__(kConsumerThreads, 1) window_kernel_direct(LayerDev L, WindowBufs W, KernelCfg C) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ volatile int s_abort;
+  __shared__ SPlan sp;
+  const Smem m = carve(smem, C);
+  const Ring rg{m.ring, m.full, m.empty, &s_abort};
+  init_cta(C, m, &s_abort);
+  for (int i = threadIdx.x; i < 2 * kMaxExperts; i += blockDim.x) (&sp.wcnt[0][0])[i] = 0;
+  router_stage<BITS>(L, W, reinterpret_cast<float*>(m.ring));
+  if (!grid_barrier(W, &sp.ok)) return;  // timed out: the error word says so
+  RingPos rp;
+  int buf = 0;
+  if (!moe_block<BITS, true>(L, W, C, sp, rg, m, rp, buf)) return;
+  if (W.T >= kGridCombineRows) {
+    if (!grid_barrier(W, &sp.ok) || s_abort) return;
+    combine_all(L, W);
   }
 }
 
@@ -1671,20 +1948,49 @@ KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit) {
   int st = C.stage_bytes > 0 ? ring / C.stage_bytes : 0;
   C.nstages = st > kMaxStages ? kMaxStages : st;
   C.total_bytes = C.nstages * C.stage_bytes + fixed;
+  C.direct = 0;
   return C;
 }
 
-static const void* window_fn(int bits) {
+// The window kernel's register-fed configuration: no stage ring, only stage
+// R's staged rows of x in its place.  Usable when every warp gets at least one
+// k-step of every task (phase 0: K = d over up to 8 warps; phase 1: K = F or
+// Fs over up to 8 warps) and the down matrix splits into 2-tile tasks.
+KernelCfg window_cfg_direct(const LayerDev& L, int max_rows, int smem_limit) {
+  KernelCfg C = window_cfg(L, max_rows, smem_limit);
+  const int kstep = L.bits == 4 ? 64 : 128;
+  // measured: faster than the ring for 2-bit layers only (their k-steps carry
+  // twice the arithmetic, and their wide activations leave a short ring)
+  const bool ok = L.bits == 2 && L.dq == 0 && L.d / kstep >= 8 && L.F / kstep >= 8 && (L.Fs == 0 || L.Fs / kstep >= 8) &&
+                  (L.d / 16) % 2 == 0 && std::getenv("STRATA_WINDOW_RING") == nullptr;
+  if (!ok) return C;
+  const int fixed = C.total_bytes - C.nstages * C.stage_bytes;
+  // the ring's place holds stage R's staged rows of x, later the warps' FIFOs
+  const int fifo = kConsumerWarps * 4 * (L.bits == 4 ? 576 : 768);
+  const int region = fifo > kMaxRows * kRouterCols * 4 ? fifo : kMaxRows * kRouterCols * 4;
+  if (region + fixed > smem_limit) return C;
+  C.direct = 1;
+  C.nstages = 1;
+  C.stage_bytes = region;
+  C.total_bytes = C.stage_bytes + fixed;
+  C.ph[0].max_sub = 4;
+  C.ph[1].max_sub = 4;
+  return C;
+}
+
+static const void* window_fn(int bits, int direct) {
+  if (direct) return (const void*)window_kernel_direct<2>;
   return bits == 4 ? (const void*)window_kernel<4> : (const void*)window_kernel<2>;
 }
 
-cudaError_t window_set_attrs(int bits, int smem_bytes) {
-  return cudaFuncSetAttribute(window_fn(bits), cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+cudaError_t window_set_attrs(int bits, int direct, int smem_bytes) {
+  return cudaFuncSetAttribute(window_fn(bits, direct), cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
-int window_blocks_per_sm(int bits, int smem_bytes) {
+int window_blocks_per_sm(int bits, int direct, int smem_bytes) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, window_fn(bits), kExpertThreads, smem_bytes) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, window_fn(bits, direct), direct ? kConsumerThreads : kExpertThreads,
+                                                    smem_bytes) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1694,7 +2000,7 @@ int window_blocks_per_sm(int bits, int smem_bytes) {
 cudaError_t launch_window(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, int grid, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kExpertThreads);
+  cfg.blockDim = dim3(C.direct ? kConsumerThreads : kExpertThreads);
   cfg.dynamicSmemBytes = C.total_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1702,6 +2008,7 @@ cudaError_t launch_window(const LayerDev& L, const WindowBufs& W, const KernelCf
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (C.direct) return cudaLaunchKernelEx(&cfg, window_kernel_direct<2>, L, W, C);
   if (L.bits == 4) return cudaLaunchKernelEx(&cfg, window_kernel<4>, L, W, C);
   return cudaLaunchKernelEx(&cfg, window_kernel<2>, L, W, C);
 }

@@ -162,3 +162,32 @@ def test_forward_argument_errors_on_device_handle():
     assert st == B.STRATA_OK and info.n_sm > 0 and info.stages >= 2 and info.smem_bytes > 0
     assert info.expert_bytes == layer.expert_bytes and info.shared_bytes == layer.shared_bytes
     assert B.strata_window_sync(win.handle) == B.STRATA_OK
+
+
+# A 2-bit layer large enough for the warp-streamed window path (every warp
+# gets at least one 128-column k-step of each task: d, F and the shared width
+# of at least 8 k-steps), small enough for full oracle checks; shared routing
+# (few experts) mixes one- and many-row groups in the same window.
+WIDE2 = small_spec(hidden=1024, n_experts=12, top_k=4, ffn=1024, shared_ffn=1024, bits=2, block=16)
+
+
+@pytest.mark.parametrize("T", [1, 3, 6, 8])
+def test_two_bit_streamed_path(T):
+    wl, layer, ol, win = _setup(spec=WIDE2)
+    assert win.info().stages == 1  # the warp-streamed configuration holds no stage ring
+    _check(win, ol, _window(wl, ol, T, window=T))
+
+
+def test_two_bit_streamed_path_entry_points_agree():
+    from slot_decode_window_gb300 import binding as B
+    wl, layer, ol, win = _setup(spec=WIDE2)
+    for T in (2, 8):
+        x = torch.from_numpy(_window(wl, ol, T, window=50 + T)).cuda()
+        y0 = win.forward(x)
+        yg = torch.empty_like(x)
+        win.forward_graph(x, yg)
+        yn = torch.full_like(x, float("nan"))
+        assert B.strata_moe_window_forward_noalloc(win.handle, x.data_ptr(), T, yn.data_ptr()) == B.STRATA_OK
+        win.sync()
+        assert torch.equal(y0, yg)
+        assert torch.equal(y0, yn)
