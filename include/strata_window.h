@@ -104,8 +104,9 @@ typedef struct {
 /* Sizes a handle chose (for measurement and tests). */
 typedef struct {
   int32_t n_sm;               /* SMs of the device (CTAs of the window kernel) */
-  int32_t stages;             /* shared-memory ring stages of the window kernel */
-  int32_t stage_bytes;        /* bytes per ring stage */
+  int32_t stages;             /* shared-memory ring stages of the window kernel; 1 when the handle uses the
+                                 warp-streamed path (2-bit layers: no ring, per-warp copy FIFOs) */
+  int32_t stage_bytes;        /* bytes per ring stage (warp-streamed path: the FIFO region) */
   int32_t smem_bytes;         /* dynamic shared memory bytes per CTA */
   int64_t packed_bytes;       /* bytes of the handle's kernel-ordered weights */
   int64_t expert_bytes;       /* block-format bytes of one routed expert (gate+up+down) */
