@@ -295,6 +295,10 @@ def run_ours(args, rank, world, local_rank):
         return
 
     if args.mode == "windows":
+        # the handle holds its own packed copy: free the unpacked tensors so a
+        # profiler capture of a large layer keeps only that copy on the device
+        del layer
+        torch.cuda.empty_cache()
         T = args.rows
         xw = torch.from_numpy(np.stack([wlm.make_window(wl, T, seed=0, window=w) for w in range(N_WINDOWS)])).to(dev)
         yw = torch.empty(T, d, device=dev)
