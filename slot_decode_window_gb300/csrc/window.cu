@@ -304,7 +304,6 @@ struct SPlan {
   int wscan[32];
   int wcnt[2][kMaxExperts];         // per-warp expert counts of the grouping pass
   int finish[kMaxEntries * 4];      // row slices this CTA combines
-  int fifo_tag[kConsumerWarps][8];  // warp-streamed path: the items in each warp's FIFO slots
   int nfinish;
   int ok;                           // the grid barrier passed
   PhaseTasks pt[4];                 // gate/up, down, dense q/k/v, dense o
@@ -1273,8 +1272,6 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
 // of each task into a private FIFO of shared-memory slots with 16-byte
 // cp.async, kDepth items ahead; no producer warp and no CTA-wide stage ring
 // ---------------------------------------------------------------------------
-enum : int { kItemK = 1, kItemM = 2, kItemFirst = 4, kItemLast = 8 };
-
 // FIFO depth in items (the path is used for 2-bit layers)
 template <int BITS> struct FifoDepth { static constexpr int value = 4; };
 
@@ -1282,78 +1279,92 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// A warp's item stream over its CTA's task range of one phase: in each task
-// the warp takes k-steps [k0, k1) and min groups [m0, m1) of sub-tile `sub`
-// (k-steps first).  An item is one k-step chunk (512 code bytes and the scale
-// records, laid out as in the tile) or one 512-byte min fragment.  Every
-// warp has at least one item in every task (the kernel is used only when each
-// warp's k-range is non-empty).
+// A warp's items of one task of contraction length K: k-steps [k0, k0 + nk)
+// then min groups [m0, m0 + n - nk) of its sub-tile.  An item is one k-step
+// chunk (512 code bytes and the scale records, laid out as in the tile) or one
+// 512-byte min fragment.  The copying side and the computing side of a warp
+// both take the ranges from here, so they walk the same item sequence.
+struct ItemRange {
+  int k0, nk, m0, n;
+};
+template <int BITS, int NS>
+__device__ __forceinline__ ItemRange item_range(int K, int kg) {
+  constexpr int kWPS = kConsumerWarps / NS;
+  const int nks = K / Fmt<BITS>::kKstep, nmk = (K / Fmt<BITS>::kBlock + 15) / 16;
+  ItemRange r;
+  r.k0 = kg * nks / kWPS;
+  r.nk = (kg + 1) * nks / kWPS - r.k0;
+  r.m0 = kg * nmk / kWPS;
+  r.n = r.nk + (kg + 1) * nmk / kWPS - r.m0;
+  return r;
+}
+
+template <int PHASE>
+__device__ __forceinline__ int task_k(const LayerDev& L, const Task& tk) {
+  return PHASE == 0 ? L.d : (tk.shared ? L.Fs : L.F);
+}
+
+// The copying side of a warp's item stream over its CTA's task range of one
+// phase.  Every warp has at least one item in every task (the kernel is used
+// only when each warp's k-range is non-empty).
 template <int BITS, int PHASE, int NS>
 struct DStream {
   static constexpr int kMT = PHASE == 0 ? NS / 2 : NS;
-  static constexpr int kWPS = kConsumerWarps / NS;
   TaskWalk tw;
-  int task, t1, i, n, nk, k0, m0, nks;
-  const uint8_t* tile;
+  int task, t1, i, n, nk;
+  const uint8_t* kp;  // the next k-step chunk of the current task
+  const uint8_t* mp;  // the next min fragment
+  volatile int* abort_flag;
 
-  __device__ __forceinline__ void set(const LayerDev& L, int sub, int kg, volatile int* abort_flag, unsigned* err) {
+  __device__ __forceinline__ void set(const LayerDev& L, int sub, int kg, unsigned* err) {
     const Task& tk = tw.tk;
     if (!tk.shared && (unsigned)tk.expert >= (unsigned)L.E) {  // only with a corrupt plan
       atomicOr(err, kErrIndex);
-      *abort_flag = 1;
-      task = t1;
+      *abort_flag = 1;  // later waits give up at once
+      task = t1;        // no further copies; the computing side stops at this task
       return;
     }
-    const int K = PHASE == 0 ? L.d : (tk.shared ? L.Fs : L.F);
-    nks = K / Fmt<BITS>::kKstep;
-    const int nmk = (K / Fmt<BITS>::kBlock + 15) / 16;
-    k0 = kg * nks / kWPS;
-    const int k1 = (kg + 1) * nks / kWPS;
-    m0 = kg * nmk / kWPS;
-    const int m1 = (kg + 1) * nmk / kWPS;
-    nk = k1 - k0;
-    n = nk + (m1 - m0);
+    const int K = task_k<PHASE>(L, tk);
+    const ItemRange r = item_range<BITS, NS>(K, kg);
+    const int nks = K / Fmt<BITS>::kKstep, nmk = (K / Fmt<BITS>::kBlock + 15) / 16;
     const int tbytes = nks * Fmt<BITS>::kChunk + nmk * 512;
     const MatRef M = task_mat<PHASE, kMT>(L, tk.shared, sub);
     const int t = tk.tile + (PHASE == 0 && sub >= kMT ? sub - kMT : sub);
-    tile = M.base + (tk.shared ? 0LL : (long long)tk.expert * M.mat_bytes) + (long long)t * tbytes;
+    const uint8_t* tile = M.base + (tk.shared ? 0LL : (long long)tk.expert * M.mat_bytes) + (long long)t * tbytes;
+    kp = tile + (size_t)r.k0 * Fmt<BITS>::kChunk;
+    mp = tile + (size_t)nks * Fmt<BITS>::kChunk + (size_t)r.m0 * 512;
+    nk = r.nk;
+    n = r.n;
     i = 0;
   }
   __device__ __forceinline__ void start(const LayerDev& L, const SPlan& sp, const PhaseTasks& pt, int sub, int kg,
-                                        volatile int* abort_flag, unsigned* err) {
+                                        volatile int* abort, unsigned* err) {
+    abort_flag = abort;
     task = pt.t0;
     t1 = pt.t1;
     if (task < t1) {
       tw.start(task, pt, L.Fs > 0, sp);
-      set(L, sub, kg, abort_flag, err);
+      set(L, sub, kg, err);
     }
   }
-  // copy the next item into `dst` (this warp's slot; not waited for) and
-  // return its tag: bit 0 k-step, bit 1 min group, bit 2 first item of its
-  // task, bit 3 last item, bits 4.. the k-step or min-group index; 0 = none
-  __device__ __forceinline__ int issue(uint8_t* dst, const LayerDev& L, const SPlan& sp, const PhaseTasks& pt,
-                                       int sub, int kg, int lane, volatile int* abort_flag, unsigned* err) {
-    if (task >= t1) return 0;
-    int tag = (i == 0 ? kItemFirst : 0) | (i == n - 1 ? kItemLast : 0);
+  // copy the next item into `dst` (this warp's slot; not waited for); past
+  // the range's last item nothing is copied
+  __device__ __forceinline__ void issue(uint8_t* dst, const LayerDev& L, const SPlan& sp, const PhaseTasks& pt,
+                                        int sub, int kg, int lane, unsigned* err) {
+    if (task >= t1) return;
     if (i < nk) {
       constexpr int kScaleBytes = Fmt<BITS>::kChunk - 512;
-      const int ks = k0 + i;
-      const uint8_t* p = tile + (size_t)ks * Fmt<BITS>::kChunk;
-      cp_async16(dst + lane * 16, p + lane * 16);
-      if (lane * 16 < kScaleBytes) cp_async16(dst + 512 + lane * 16, p + 512 + lane * 16);
-      tag |= kItemK | (ks << 4);
+      cp_async16(dst + lane * 16, kp + lane * 16);
+      if (lane * 16 < kScaleBytes) cp_async16(dst + 512 + lane * 16, kp + 512 + lane * 16);
+      kp += Fmt<BITS>::kChunk;
     } else {
-      const int mk = m0 + (i - nk);
-      cp_async16(dst + lane * 16, tile + (size_t)nks * Fmt<BITS>::kChunk + mk * 512 + lane * 16);
-      tag |= kItemM | (mk << 4);
+      cp_async16(dst + lane * 16, mp + lane * 16);
+      mp += 512;
     }
-    if (++i == n) {
-      if (++task < t1) {
-        tw.next(pt, L.Fs > 0, sp);
-        set(L, sub, kg, abort_flag, err);
-      }
+    if (++i == n && ++task < t1) {
+      tw.next(pt, L.Fs > 0, sp);
+      set(L, sub, kg, err);
     }
-    return tag;
   }
 };
 
@@ -1361,81 +1372,77 @@ struct DStream {
 // kDepth items of its stream in flight in its FIFO slots (one cp.async group
 // per item); items are consumed in order, across task and group boundaries,
 // so a phase's first copies are in flight while its first group's
-// activations are staged.
+// activations are staged.  The computing side tracks its own place in each
+// task's item range.  After an abort (a timed-out wait) the warps still walk
+// every task, so that all of them meet every barrier; the results are then
+// discarded by the caller through the error word.
 template <int BITS, int PHASE, int NS>
 __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, SPlan& sp,
                                volatile int* abort_flag, __half* bm, __half* bs, float4* red, uint8_t* fifo,
                                int& buf) {
-  constexpr int kWPS = kConsumerWarps / NS;
   constexpr int kDepth = FifoDepth<BITS>::value;
   constexpr int kSlot = Fmt<BITS>::kChunk;
   constexpr int S = Fmt<BITS>::kBHalves;
+  constexpr int kWPS = kConsumerWarps / NS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PhaseTasks& pt = sp.pt[PHASE];
   const bool has_shared = L.Fs > 0;
   const int sub = warp / kWPS, kg = warp % kWPS;
   if (pt.t0 < pt.t1) {
-    uint8_t* slots = fifo + (size_t)warp * kDepth * kSlot;
-    int* tags = sp.fifo_tag[warp];
+    uint8_t* const slots = fifo + (size_t)warp * kDepth * kSlot;
+    uint8_t* const slots_end = slots + kDepth * kSlot;
     DStream<BITS, PHASE, NS> ds;
     ds.start(L, sp, pt, sub, kg, abort_flag, W.err);
 #pragma unroll
     for (int q = 0; q < kDepth; ++q) {
-      const int tg = ds.issue(slots + q * kSlot, L, sp, pt, sub, kg, lane, abort_flag, W.err);
-      if (lane == 0) tags[q] = tg;
+      ds.issue(slots + q * kSlot, L, sp, pt, sub, kg, lane, W.err);
       cp_async_commit();
     }
     GroupState gs;
     TaskWalk tw;
     tw.start(pt.t0, pt, has_shared, sp);
-    int task = pt.t0, slot = 0;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
+    int task = pt.t0;
+    uint8_t* it = slots;
     while (true) {
-      cp_async_wait_group<kDepth - 1>();  // this lane's copies of the oldest item have landed
-      __syncwarp();
-      const int tag = tags[slot];
-      if (tag == 0) break;
-      const uint8_t* it = slots + slot * kSlot;
       const Task& tk = tw.tk;
-      if (tag & kItemFirst) {
-        const int K = PHASE == 0 ? L.d : (tk.shared ? L.Fs : L.F);
-        if (tk.group != gs.cur) enter_group<BITS, PHASE>(L, W, C, sp, tk, K, abort_flag, bm, bs, gs);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = accm[q] = 0.f;
-      }
-      if (!*abort_flag) {
-        const int idx = tag >> 4;
-        if (tag & kItemK) {
-          const __half* bk = bm + idx * 32 * S + gs.lane_b * 8;
+      if (!tk.shared && (unsigned)tk.expert >= (unsigned)L.E) break;  // flagged by the copying side
+      const int K = task_k<PHASE>(L, tk);
+      if (tk.group != gs.cur) enter_group<BITS, PHASE>(L, W, C, sp, tk, K, abort_flag, bm, bs, gs);
+      const ItemRange r = item_range<BITS, NS>(K, kg);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
+      const __half* bk = bm + r.k0 * 32 * S + gs.lane_b * 8;
+      const __half* bsm = bs + r.m0 * 128 + gs.lane_b * 4;
+      for (int ci = 0; ci < r.n; ++ci) {
+        cp_async_wait_group<kDepth - 1>();  // this lane's copies of the oldest item have landed
+        __syncwarp();
+        if (ci < r.nk) {
           if (gs.paired) kstep_mma<BITS, true>(it, bk, C.bmain_halves, lane, acc);
           else kstep_mma<BITS, false>(it, bk, C.bmain_halves, lane, acc);
+          bk += 32 * S;
         } else {
           const uint4 am = *reinterpret_cast<const uint4*>(it + lane * 16);
-          const uint2 b = *reinterpret_cast<const uint2*>(bs + idx * 128 + gs.lane_b * 4);
+          const uint2 b = *reinterpret_cast<const uint2*>(bsm);
           mma16816(accm, am.x, am.y, am.z, am.w, b.x, b.y, accm);
           if (!gs.paired) {
-            const uint2 l = *reinterpret_cast<const uint2*>(bs + C.bsum_halves + idx * 128 + gs.lane_b * 4);
+            const uint2 l = *reinterpret_cast<const uint2*>(bsm + C.bsum_halves);
             mma16816(accm, am.x, am.y, am.z, am.w, l.x, l.y, accm);
           }
+          bsm += 128;
         }
-      }
-      __syncwarp();  // every lane is done with the slot before it is refilled
-      {
-        const int tg = ds.issue(slots + slot * kSlot, L, sp, pt, sub, kg, lane, abort_flag, W.err);
-        if (lane == 0) tags[slot] = tg;
+        __syncwarp();  // every lane is done with the slot before it is refilled
+        ds.issue(it, L, sp, pt, sub, kg, lane, W.err);
         cp_async_commit();
+        it += kSlot;
+        if (it == slots_end) it = slots;
       }
-      slot = slot + 1 == kDepth ? 0 : slot + 1;
-      if (tag & kItemLast) {
-        float4* rb = red + buf * (kConsumerWarps * 32);
-        rb[warp * 32 + lane] = make_float4(fmaf(acc[0], kDqUnscale, accm[0]), fmaf(acc[1], kDqUnscale, accm[1]),
-                                           fmaf(acc[2], kDqUnscale, accm[2]), fmaf(acc[3], kDqUnscale, accm[3]));
-        consumer_sync();
-        task_epilogue<BITS, PHASE, NS>(L, W, sp, rb, tk, task, gs);
-        buf ^= 1;
-        if (++task == pt.t1) break;
-        tw.next(pt, has_shared, sp);
-      }
+      float4* rb = red + buf * (kConsumerWarps * 32);
+      rb[warp * 32 + lane] = make_float4(fmaf(acc[0], kDqUnscale, accm[0]), fmaf(acc[1], kDqUnscale, accm[1]),
+                                         fmaf(acc[2], kDqUnscale, accm[2]), fmaf(acc[3], kDqUnscale, accm[3]));
+      consumer_sync();
+      task_epilogue<BITS, PHASE, NS>(L, W, sp, rb, tk, task, gs);
+      buf ^= 1;
+      if (++task == pt.t1) break;
+      tw.next(pt, has_shared, sp);
     }
     cp_async_wait_all();  // nothing of this phase may land in the FIFO later
     __syncwarp();
