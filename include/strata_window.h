@@ -105,7 +105,8 @@ typedef struct {
 typedef struct {
   int32_t n_sm;               /* SMs of the device (CTAs of the window kernel) */
   int32_t stages;             /* shared-memory ring stages of the window kernel; 1 when the handle uses the
-                                 warp-streamed path (2-bit layers: no ring, per-warp copy FIFOs) */
+                                 warp-streamed path (no ring, per-warp copy FIFOs: 2-bit layers, and 4-bit
+                                 layers whose activations leave a ring under three 32 KB stages) */
   int32_t stage_bytes;        /* bytes per ring stage (warp-streamed path: the FIFO region) */
   int32_t smem_bytes;         /* dynamic shared memory bytes per CTA */
   int64_t packed_bytes;       /* bytes of the handle's kernel-ordered weights */

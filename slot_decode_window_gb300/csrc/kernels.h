@@ -8,7 +8,8 @@ constexpr int kRouterCols = 512;  // columns per router partial-logit chunk
 
 // Shared-memory plan of the window kernel for one layer shape.
 KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit);
-// The same with the register-fed path when the shape allows it (C.direct).
+// The same with the warp-streamed path (C.direct) where it is the faster one
+// and the shape allows it.
 KernelCfg window_cfg_direct(const LayerDev& L, int max_rows, int smem_limit);
 cudaError_t window_set_attrs(int bits, int direct, int smem_bytes);
 // CTAs of the window kernel that one SM holds (0 if it does not fit).

@@ -1272,7 +1272,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
 // of each task into a private FIFO of shared-memory slots with 16-byte
 // cp.async, kDepth items ahead; no producer warp and no CTA-wide stage ring
 // ---------------------------------------------------------------------------
-// FIFO depth in items (the path is used for 2-bit layers)
+// FIFO depth in items per warp
 template <int BITS> struct FifoDepth { static constexpr int value = 4; };
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -1412,28 +1412,45 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
       float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
       const __half* bk = bm + r.k0 * 32 * S + gs.lane_b * 8;
       const __half* bsm = bs + r.m0 * 128 + gs.lane_b * 4;
-      for (int ci = 0; ci < r.n; ++ci) {
-        cp_async_wait_group<kDepth - 1>();  // this lane's copies of the oldest item have landed
-        __syncwarp();
-        if (ci < r.nk) {
-          if (gs.paired) kstep_mma<BITS, true>(it, bk, C.bmain_halves, lane, acc);
-          else kstep_mma<BITS, false>(it, bk, C.bmain_halves, lane, acc);
-          bk += 32 * S;
-        } else {
-          const uint4 am = *reinterpret_cast<const uint4*>(it + lane * 16);
-          const uint2 b = *reinterpret_cast<const uint2*>(bsm);
-          mma16816(accm, am.x, am.y, am.z, am.w, b.x, b.y, accm);
-          if (!gs.paired) {
-            const uint2 l = *reinterpret_cast<const uint2*>(bsm + C.bsum_halves);
-            mma16816(accm, am.x, am.y, am.z, am.w, l.x, l.y, accm);
-          }
-          bsm += 128;
-        }
+      // refill the slot just used with the stream's next item, then move on
+      auto next_slot = [&]() {
         __syncwarp();  // every lane is done with the slot before it is refilled
         ds.issue(it, L, sp, pt, sub, kg, lane, W.err);
         cp_async_commit();
         it += kSlot;
         if (it == slots_end) it = slots;
+      };
+      // k-steps first, then min groups; the item's copies are this lane's
+      // oldest group in flight
+      if (gs.paired) {
+        for (int ci = 0; ci < r.nk; ++ci) {
+          cp_async_wait_group<kDepth - 1>();
+          __syncwarp();
+          kstep_mma<BITS, true>(it, bk, C.bmain_halves, lane, acc);
+          bk += 32 * S;
+          next_slot();
+        }
+      } else {
+        for (int ci = 0; ci < r.nk; ++ci) {
+          cp_async_wait_group<kDepth - 1>();
+          __syncwarp();
+          kstep_mma<BITS, false>(it, bk, C.bmain_halves, lane, acc);
+          bk += 32 * S;
+          next_slot();
+        }
+      }
+      for (int ci = r.nk; ci < r.n; ++ci) {
+        cp_async_wait_group<kDepth - 1>();
+        __syncwarp();
+        const uint4 am = *reinterpret_cast<const uint4*>(it + lane * 16);
+        const uint2 b = *reinterpret_cast<const uint2*>(bsm);
+        mma16816(accm, am.x, am.y, am.z, am.w, b.x, b.y, accm);
+        if (!gs.paired) {
+          const uint2 l = *reinterpret_cast<const uint2*>(bsm + C.bsum_halves);
+          mma16816(accm, am.x, am.y, am.z, am.w, l.x, l.y, accm);
+        }
+        bsm += 128;
+        next_slot();
       }
       float4* rb = red + buf * (kConsumerWarps * 32);
       rb[warp * 32 + lane] = make_float4(fmaf(acc[0], kDqUnscale, accm[0]), fmaf(acc[1], kDqUnscale, accm[1]),
@@ -1966,10 +1983,17 @@ KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit) {
 KernelCfg window_cfg_direct(const LayerDev& L, int max_rows, int smem_limit) {
   KernelCfg C = window_cfg(L, max_rows, smem_limit);
   const int kstep = L.bits == 4 ? 64 : 128;
-  // measured: faster than the ring for 2-bit layers only (their k-steps carry
-  // twice the arithmetic, and their wide activations leave a short ring)
-  const bool ok = L.bits == 2 && L.dq == 0 && L.d / kstep >= 8 && L.F / kstep >= 8 && (L.Fs == 0 || L.Fs / kstep >= 8) &&
-                  (L.d / 16) % 2 == 0 && std::getenv("STRATA_WINDOW_RING") == nullptr;
+  // measured: faster than the ring for 2-bit layers (their k-steps carry
+  // twice the arithmetic) and for 4-bit layers whose wide activations leave a
+  // ring of less than three 32 KB stages (d = 4096: 115 against 123 us per
+  // eight-row window); the ring wins where it is longer (d = 2048: 74 against
+  // 84 us).  STRATA_WINDOW_RING=1 forces the ring and STRATA_WINDOW_DIRECT=1
+  // this path wherever its shape conditions hold, for comparisons and tests.
+  const bool short_ring = C.nstages * C.stage_bytes < 96 * 1024;
+  const bool force = std::getenv("STRATA_WINDOW_DIRECT") != nullptr;
+  const bool ok = (L.bits == 2 || short_ring || force) && L.dq == 0 && L.d / kstep >= 8 && L.F / kstep >= 8 &&
+                  (L.Fs == 0 || L.Fs / kstep >= 8) && (L.d / 16) % 2 == 0 &&
+                  std::getenv("STRATA_WINDOW_RING") == nullptr;
   if (!ok) return C;
   const int fixed = C.total_bytes - C.nstages * C.stage_bytes;
   // the ring's place holds stage R's staged rows of x, later the warps' FIFOs
@@ -1986,7 +2010,7 @@ KernelCfg window_cfg_direct(const LayerDev& L, int max_rows, int smem_limit) {
 }
 
 static const void* window_fn(int bits, int direct) {
-  if (direct) return (const void*)window_kernel_direct<2>;
+  if (direct) return bits == 4 ? (const void*)window_kernel_direct<4> : (const void*)window_kernel_direct<2>;
   return bits == 4 ? (const void*)window_kernel<4> : (const void*)window_kernel<2>;
 }
 
@@ -2015,7 +2039,9 @@ cudaError_t launch_window(const LayerDev& L, const WindowBufs& W, const KernelCf
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (C.direct) return cudaLaunchKernelEx(&cfg, window_kernel_direct<2>, L, W, C);
+  if (C.direct)
+    return L.bits == 4 ? cudaLaunchKernelEx(&cfg, window_kernel_direct<4>, L, W, C)
+                       : cudaLaunchKernelEx(&cfg, window_kernel_direct<2>, L, W, C);
   if (L.bits == 4) return cudaLaunchKernelEx(&cfg, window_kernel<4>, L, W, C);
   return cudaLaunchKernelEx(&cfg, window_kernel<2>, L, W, C);
 }

@@ -191,3 +191,47 @@ def test_two_bit_streamed_path_entry_points_agree():
         win.sync()
         assert torch.equal(y0, yg)
         assert torch.equal(y0, yn)
+
+
+# A 4-bit layer at the smallest width where every warp of the warp-streamed
+# path gets a 64-column k-step of each task.  At this width the ring is long,
+# so the handle would take the ring path; STRATA_WINDOW_DIRECT=1 at creation
+# forces the warp-streamed one (which 4-bit layers take when their activations
+# leave a short ring, as at d = 4096).
+WIDE4 = small_spec(hidden=512, n_experts=12, top_k=4, ffn=512, shared_ffn=512)
+
+
+def _forced_direct(spec, seed=5):
+    import os
+    os.environ["STRATA_WINDOW_DIRECT"] = "1"
+    try:
+        return _setup(spec=spec, seed=seed)
+    finally:
+        del os.environ["STRATA_WINDOW_DIRECT"]
+
+
+@pytest.mark.parametrize("T", [1, 3, 6, 8])
+def test_four_bit_streamed_path(T):
+    wl, layer, ol, win = _forced_direct(WIDE4)
+    assert win.info().stages == 1
+    _check(win, ol, _window(wl, ol, T, window=T))
+
+
+def test_four_bit_paths_agree_and_wide_layer_streams():
+    """The forced warp-streamed handle and a ring handle of the same layer agree
+    within the tolerance; a d = 4096 4-bit layer takes the streamed path."""
+    from slot_decode_window_gb300.binding import Window
+    wl, layer, ol, win = _forced_direct(WIDE4)
+    ring = Window(layer, max_rows=8)
+    try:
+        assert ring.info().stages >= 2
+        x = torch.from_numpy(_window(wl, ol, 8, window=21)).cuda()
+        yd, yr = win.forward(x), ring.forward(x)
+        win.sync()
+        ring.sync()
+        rms = float(torch.sqrt(torch.mean(yr.double() ** 2)))
+        assert float((yd - yr).abs().max()) <= TOL * rms
+    finally:
+        ring.close()
+    wz, _, _, winz = _setup("zipf")
+    assert winz.info().stages == 1
