@@ -1128,20 +1128,42 @@ __device__ __forceinline__ void enter_group(const LayerDev& L, const WindowBufs&
   gs.cur = tk.group;
 }
 
-// One task's epilogue: the cross-warp sums of its partials (rb) in a fixed
-// order, on consecutive threads of one or two warps rotating with the task.
+// The warps that share a task's outputs: in gate/up (phase 0) row tile m's
+// gate and up sub-tiles, in the other phases one sub-tile.  After each task
+// they meet at their own named barrier (ids 2..5) and sum its partials among
+// themselves, so the warps of other row tiles go on without waiting.  Warps
+// of all groups still meet before a group's activations are restaged.
+template <int PHASE, int NS>
+struct OutGroup {
+  static constexpr int kWPS = kConsumerWarps / NS;
+  static constexpr int kMT = PHASE == 0 ? NS / 2 : NS;
+  static constexpr int kThreads = (PHASE == 0 ? 2 * kWPS : kWPS) * 32;
+  int id;    // row tile (phase 0) or sub-tile
+  int gtid;  // thread index inside the group
+  __device__ __forceinline__ OutGroup(int sub, int kg, int lane) {
+    id = PHASE == 0 ? sub % kMT : sub;
+    gtid = (PHASE == 0 && sub >= kMT ? kWPS * 32 : 0) + kg * 32 + lane;
+  }
+  __device__ __forceinline__ void sync() const {
+    asm volatile("bar.sync %0, %1;" ::"r"(2 + id), "n"(kThreads) : "memory");
+  }
+};
+
+// One task's epilogue over the outputs of group og: the cross-warp sums of
+// its partials (rb) in a fixed order, on consecutive threads of the group,
+// starting at a warp that rotates with the task.
 template <int BITS, int PHASE, int NS>
 __device__ __forceinline__ void task_epilogue(const LayerDev& L, const WindowBufs& W, const SPlan& sp,
-                                              const float4* rb, const Task& tk, int task, const GroupState& gs) {
+                                              const float4* rb, const Task& tk, int task, const GroupState& gs,
+                                              const OutGroup<PHASE, NS>& og) {
   constexpr int kMT = PHASE == 0 ? NS / 2 : NS;
   constexpr int kWPS = kConsumerWarps / NS;
-  const int tid = threadIdx.x, lane = tid & 31;
-  // ---------------- epilogue: cross-warp sums in a fixed order ----------------
-  // outputs on consecutive threads of one or two warps, rotating with the task,
-  // so the other warps go straight on to the next task
-  const int eo = (tid + 32 * (task & (kConsumerWarps - 1))) & (kConsumerThreads - 1);
+  constexpr int kGT = OutGroup<PHASE, NS>::kThreads;
+  const int lane = threadIdx.x & 31;
+  const int i0 = og.id * 16 * gs.R, i1 = i0 + 16 * gs.R;
+  const int eo = (og.gtid + 32 * task) & (kGT - 1);
   if (PHASE == 0) {
-    for (int i = eo; i < kMT * 16 * gs.R; i += kConsumerThreads) {
+    for (int i = i0 + eo; i < i1; i += kGT) {
       const int m = (int)(((uint32_t)i * gs.inv_d) >> 16), rem = i - m * 16 * gs.R;
       const int r = rem >> 4, row = rem & 15;
       const int src_lane = (row & 7) * 4 + (gs.paired ? r : (r >> 1));
@@ -1174,7 +1196,7 @@ __device__ __forceinline__ void task_epilogue(const LayerDev& L, const WindowBuf
       if (row == 0) (tk.shared ? W.shsum : W.hsum)[hrow * (Kh / 16) + f / 16] = ps;
     }
   } else {
-    for (int i = eo; i < NS * 16 * gs.R; i += kConsumerThreads) {
+    for (int i = i0 + eo; i < i1; i += kGT) {
       const int s = (int)(((uint32_t)i * gs.inv_d) >> 16), rem = i - s * 16 * gs.R;
       const int r = rem >> 4, row = rem & 15;
       const int src_lane = (row & 7) * 4 + (gs.paired ? r : (r >> 1));
@@ -1213,6 +1235,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
   const PhaseTasks& pt = sp.pt[PHASE];
   const bool has_shared = L.Fs > 0;
   const int sub = warp / kWPS, kg = warp % kWPS;
+  const OutGroup<PHASE, NS> og(sub, kg, lane);
   GroupState gs;
   TaskWalk tw;
   if (pt.t0 < pt.t1) tw.start(pt.t0, pt, has_shared, sp);
@@ -1220,7 +1243,10 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
     const Task& tk = tw.tk;
     if (!tk.shared && (unsigned)tk.expert >= (unsigned)L.E) break;  // flagged by the producer
     const int K = PHASE == 0 ? L.d : PHASE == 1 ? (tk.shared ? L.Fs : L.F) : PHASE == 2 ? L.d : L.dq;
-    if (tk.group != gs.cur) enter_group<BITS, PHASE>(L, W, C, sp, tk, K, rg.abort_flag, bm, bs, gs);
+    if (tk.group != gs.cur) {
+      consumer_sync();  // no warp still reads the previous group's activations
+      enter_group<BITS, PHASE>(L, W, C, sp, tk, K, rg.abort_flag, bm, bs, gs);
+    }
     const int kv = (PHASE == 1 && tk.shared) ? 1 : 0;
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
     if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 0);
@@ -1250,10 +1276,10 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
     float4* rb = red + buf * (kConsumerWarps * 32);
     rb[warp * 32 + lane] = make_float4(fmaf(acc[0], kDqUnscale, accm[0]), fmaf(acc[1], kDqUnscale, accm[1]),
                                        fmaf(acc[2], kDqUnscale, accm[2]), fmaf(acc[3], kDqUnscale, accm[3]));
-    consumer_sync();
+    og.sync();
     if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 3);
 
-    task_epilogue<BITS, PHASE, NS>(L, W, sp, rb, tk, task, gs);
+    task_epilogue<BITS, PHASE, NS>(L, W, sp, rb, tk, task, gs, og);
     buf ^= 1;
   }
   if (PHASE == 0) {
@@ -1398,6 +1424,7 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
       ds.issue(slots + q * kSlot, L, sp, pt, sub, kg, lane, W.err);
       cp_async_commit();
     }
+    const OutGroup<PHASE, NS> og(sub, kg, lane);
     GroupState gs;
     TaskWalk tw;
     tw.start(pt.t0, pt, has_shared, sp);
@@ -1407,7 +1434,10 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
       const Task& tk = tw.tk;
       if (!tk.shared && (unsigned)tk.expert >= (unsigned)L.E) break;  // flagged by the copying side
       const int K = task_k<PHASE>(L, tk);
-      if (tk.group != gs.cur) enter_group<BITS, PHASE>(L, W, C, sp, tk, K, abort_flag, bm, bs, gs);
+      if (tk.group != gs.cur) {
+        consumer_sync();  // no warp still reads the previous group's activations
+        enter_group<BITS, PHASE>(L, W, C, sp, tk, K, abort_flag, bm, bs, gs);
+      }
       const ItemRange r = item_range<BITS, NS>(K, kg);
       float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
       const __half* bk = bm + r.k0 * 32 * S + gs.lane_b * 8;
@@ -1455,8 +1485,8 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
       float4* rb = red + buf * (kConsumerWarps * 32);
       rb[warp * 32 + lane] = make_float4(fmaf(acc[0], kDqUnscale, accm[0]), fmaf(acc[1], kDqUnscale, accm[1]),
                                          fmaf(acc[2], kDqUnscale, accm[2]), fmaf(acc[3], kDqUnscale, accm[3]));
-      consumer_sync();
-      task_epilogue<BITS, PHASE, NS>(L, W, sp, rb, tk, task, gs);
+      og.sync();
+      task_epilogue<BITS, PHASE, NS>(L, W, sp, rb, tk, task, gs, og);
       buf ^= 1;
       if (++task == pt.t1) break;
       tw.next(pt, has_shared, sp);
