@@ -2027,7 +2027,7 @@ KernelCfg window_cfg_direct(const LayerDev& L, int max_rows, int smem_limit) {
   if (!ok) return C;
   const int fixed = C.total_bytes - C.nstages * C.stage_bytes;
   // the ring's place holds stage R's staged rows of x, later the warps' FIFOs
-  const int fifo = kConsumerWarps * 4 * (L.bits == 4 ? 576 : 768);
+  const int fifo = kConsumerWarps * (L.bits == 4 ? FifoDepth<4>::value * Fmt<4>::kChunk : FifoDepth<2>::value * Fmt<2>::kChunk);
   const int region = fifo > kMaxRows * kRouterCols * 4 ? fifo : kMaxRows * kRouterCols * 4;
   if (region + fixed > smem_limit) return C;
   C.direct = 1;
