@@ -1129,10 +1129,13 @@ __device__ __forceinline__ void enter_group(const LayerDev& L, const WindowBufs&
 }
 
 // The warps that share a task's outputs: in gate/up (phase 0) row tile m's
-// gate and up sub-tiles, in the other phases one sub-tile.  After each task
-// they meet at their own named barrier (ids 2..5) and sum its partials among
-// themselves, so the warps of other row tiles go on without waiting.  Warps
-// of all groups still meet before a group's activations are restaged.
+// gate and up sub-tiles, in the down phase one sub-tile.  On the warp-streamed
+// path they meet after each task at their own named barrier (ids 2..5) and
+// sum its partials among themselves, so the warps of other row tiles go on
+// without waiting.  Warps of all groups still meet before a group's
+// activations are restaged.  (The ring path keeps one barrier of all 16
+// warps per task: there the groups gained nothing, and the decoder stack's
+// dense phases lost time.)
 template <int PHASE, int NS>
 struct OutGroup {
   static constexpr int kWPS = kConsumerWarps / NS;
@@ -1149,21 +1152,20 @@ struct OutGroup {
   }
 };
 
-// One task's epilogue over the outputs of group og: the cross-warp sums of
-// its partials (rb) in a fixed order, on consecutive threads of the group,
-// starting at a warp that rotates with the task.
+// One task's epilogue: the cross-warp sums of its partials (rb) in a fixed
+// order for outputs i = i_first, i_first + stride, ... < i_end (output i is
+// row r = (i mod 16R) / 16, element i mod 16 of sub-tile i / 16R).  Callers
+// hand consecutive outputs to consecutive threads, starting at a warp that
+// rotates with the task, so the other warps go straight on.
 template <int BITS, int PHASE, int NS>
 __device__ __forceinline__ void task_epilogue(const LayerDev& L, const WindowBufs& W, const SPlan& sp,
-                                              const float4* rb, const Task& tk, int task, const GroupState& gs,
-                                              const OutGroup<PHASE, NS>& og) {
+                                              const float4* rb, const Task& tk, const GroupState& gs, int i_first,
+                                              int i_end, int stride) {
   constexpr int kMT = PHASE == 0 ? NS / 2 : NS;
   constexpr int kWPS = kConsumerWarps / NS;
-  constexpr int kGT = OutGroup<PHASE, NS>::kThreads;
   const int lane = threadIdx.x & 31;
-  const int i0 = og.id * 16 * gs.R, i1 = i0 + 16 * gs.R;
-  const int eo = (og.gtid + 32 * task) & (kGT - 1);
   if (PHASE == 0) {
-    for (int i = i0 + eo; i < i1; i += kGT) {
+    for (int i = i_first; i < i_end; i += stride) {
       const int m = (int)(((uint32_t)i * gs.inv_d) >> 16), rem = i - m * 16 * gs.R;
       const int r = rem >> 4, row = rem & 15;
       const int src_lane = (row & 7) * 4 + (gs.paired ? r : (r >> 1));
@@ -1196,7 +1198,7 @@ __device__ __forceinline__ void task_epilogue(const LayerDev& L, const WindowBuf
       if (row == 0) (tk.shared ? W.shsum : W.hsum)[hrow * (Kh / 16) + f / 16] = ps;
     }
   } else {
-    for (int i = i0 + eo; i < i1; i += kGT) {
+    for (int i = i_first; i < i_end; i += stride) {
       const int s = (int)(((uint32_t)i * gs.inv_d) >> 16), rem = i - s * 16 * gs.R;
       const int r = rem >> 4, row = rem & 15;
       const int src_lane = (row & 7) * 4 + (gs.paired ? r : (r >> 1));
@@ -1235,7 +1237,6 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
   const PhaseTasks& pt = sp.pt[PHASE];
   const bool has_shared = L.Fs > 0;
   const int sub = warp / kWPS, kg = warp % kWPS;
-  const OutGroup<PHASE, NS> og(sub, kg, lane);
   GroupState gs;
   TaskWalk tw;
   if (pt.t0 < pt.t1) tw.start(pt.t0, pt, has_shared, sp);
@@ -1243,10 +1244,8 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
     const Task& tk = tw.tk;
     if (!tk.shared && (unsigned)tk.expert >= (unsigned)L.E) break;  // flagged by the producer
     const int K = PHASE == 0 ? L.d : PHASE == 1 ? (tk.shared ? L.Fs : L.F) : PHASE == 2 ? L.d : L.dq;
-    if (tk.group != gs.cur) {
-      consumer_sync();  // no warp still reads the previous group's activations
-      enter_group<BITS, PHASE>(L, W, C, sp, tk, K, rg.abort_flag, bm, bs, gs);
-    }
+    // the previous task's barrier guarantees no warp still reads the old activations
+    if (tk.group != gs.cur) enter_group<BITS, PHASE>(L, W, C, sp, tk, K, rg.abort_flag, bm, bs, gs);
     const int kv = (PHASE == 1 && tk.shared) ? 1 : 0;
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
     if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 0);
@@ -1276,10 +1275,12 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
     float4* rb = red + buf * (kConsumerWarps * 32);
     rb[warp * 32 + lane] = make_float4(fmaf(acc[0], kDqUnscale, accm[0]), fmaf(acc[1], kDqUnscale, accm[1]),
                                        fmaf(acc[2], kDqUnscale, accm[2]), fmaf(acc[3], kDqUnscale, accm[3]));
-    og.sync();
+    consumer_sync();  // all 16 warps: the ring path's warps stay in step
     if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 3);
 
-    task_epilogue<BITS, PHASE, NS>(L, W, sp, rb, tk, task, gs, og);
+    constexpr int kMT = PHASE == 0 ? NS / 2 : NS;
+    task_epilogue<BITS, PHASE, NS>(L, W, sp, rb, tk, gs, (tid + 32 * (task & (kConsumerWarps - 1))) & (kConsumerThreads - 1),
+                                   kMT * 16 * gs.R, kConsumerThreads);
     buf ^= 1;
   }
   if (PHASE == 0) {
@@ -1486,7 +1487,12 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
       rb[warp * 32 + lane] = make_float4(fmaf(acc[0], kDqUnscale, accm[0]), fmaf(acc[1], kDqUnscale, accm[1]),
                                          fmaf(acc[2], kDqUnscale, accm[2]), fmaf(acc[3], kDqUnscale, accm[3]));
       og.sync();
-      task_epilogue<BITS, PHASE, NS>(L, W, sp, rb, tk, task, gs, og);
+      {
+        constexpr int kGT = OutGroup<PHASE, NS>::kThreads;
+        const int i0 = og.id * 16 * gs.R;
+        task_epilogue<BITS, PHASE, NS>(L, W, sp, rb, tk, gs, i0 + ((og.gtid + 32 * task) & (kGT - 1)),
+                                       i0 + 16 * gs.R, kGT);
+      }
       buf ^= 1;
       if (++task == pt.t1) break;
       tw.next(pt, has_shared, sp);
