@@ -120,6 +120,12 @@ typedef struct {
  *   desc, weights: as above; weights are read on `cuda_stream` (a cudaStream_t,
  *   or NULL for the default stream) and create waits for that work to finish.
  *   out: receives the handle; set to NULL on failure.
+ * The handle picks its window kernel here (see strata_window_info.stages).
+ * Two environment variables, read at this call, override the choice for
+ * comparisons: STRATA_WINDOW_RING (any value) forces the ring path;
+ * STRATA_WINDOW_DIRECT (any value) forces the warp-streamed path where the
+ * shape allows it (every warp gets a k-step of each task).  Results of the two
+ * paths agree within the output tolerance, not bit for bit.
  * Returns EINVAL (bad pointer or shape), EUNSUPPORTED (bits/block pair or size
  * limits), ENOMEM, ECUDA. */
 strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe_weights* weights,
