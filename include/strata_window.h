@@ -131,6 +131,19 @@ typedef struct {
 strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe_weights* weights,
                                    void* cuda_stream, strata_window** out);
 
+/* The window-kernel plan a handle for this layer shape would choose, computed
+ * on the host with no device and no CUDA call: fills stages, stage_bytes and
+ * smem_bytes of *info as strata_window_query would report them (stages = 1:
+ * the warp-streamed path); every other field is set to 0.
+ *   smem_limit: dynamic shared memory the window kernel may use per CTA, in
+ *   bytes; 0 = what strata_window_create grants on a GB300 (the 232,448-byte
+ *   opt-in maximum less 12,288 bytes kept for the kernel's static shared
+ *   memory).  Create takes the device's own opt-in maximum instead.
+ * Reads the same environment overrides as strata_window_create.
+ * Returns EINVAL (NULL pointer, bad shape, negative limit) or EUNSUPPORTED
+ * (no plan fits the limit: create would fail the same way). */
+strata_status strata_window_plan(const strata_moe_desc* desc, int32_t smem_limit, strata_window_info* info);
+
 /* Run one window: y = MoE(x) for T rows.
  *   x: device fp32 [T][d], caller-owned; y: device fp32 [T][d], caller-owned,
  *   must not overlap x; both 16-byte aligned.  1 <= T <= desc.max_rows.

@@ -23,7 +23,8 @@ STRATA_OK, STRATA_EINVAL, STRATA_ENOMEM, STRATA_ECUDA, STRATA_EUNSUPPORTED, STRA
 EXPORTED = ("strata_window_create", "strata_moe_window_forward", "strata_window_sync", "strata_window_query",
             "strata_window_set_profiling", "strata_window_timings", "strata_window_destroy", "strata_status_str",
             "strata_moe_window_forward_noalloc", "strata_moe_window_forward_graph", "strata_stack_create", "strata_stack_forward", "strata_stack_sync",
-            "strata_stack_query", "strata_stack_set_profiling", "strata_stack_timings", "strata_stack_destroy")
+            "strata_stack_query", "strata_stack_set_profiling", "strata_stack_timings", "strata_stack_destroy",
+            "strata_window_plan")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -124,6 +125,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.strata_window_sync.restype = ctypes.c_int
     lib.strata_window_query.argtypes = [ctypes.c_void_p, P(strata_window_info)]
     lib.strata_window_query.restype = ctypes.c_int
+    lib.strata_window_plan.argtypes = [P(strata_moe_desc), ctypes.c_int32, P(strata_window_info)]
+    lib.strata_window_plan.restype = ctypes.c_int
     lib.strata_window_set_profiling.argtypes = [ctypes.c_void_p, ctypes.c_int32]
     lib.strata_window_set_profiling.restype = ctypes.c_int
     lib.strata_window_timings.argtypes = [ctypes.c_void_p, P(ctypes.c_float)]
@@ -215,6 +218,12 @@ def strata_window_sync(handle) -> int:
 def strata_window_query(handle):
     info = strata_window_info()
     st = load().strata_window_query(ctypes.c_void_p(handle), ctypes.byref(info))
+    return st, info
+
+
+def strata_window_plan(desc: strata_moe_desc, smem_limit: int = 0):
+    info = strata_window_info()
+    st = load().strata_window_plan(ctypes.byref(desc), smem_limit, ctypes.byref(info))
     return st, info
 
 

@@ -83,6 +83,35 @@ const char* strata_status_str(strata_status s) {
   return "unknown status";
 }
 
+// Dynamic shared memory left out of the window kernel's budget for its static
+// shared memory, and the opt-in maximum of a GB300 (227 KB) that
+// strata_window_plan assumes when given no limit.
+constexpr int kStaticSmemReserve = 12288;
+constexpr int kGb300SmemOptin = 232448;
+
+strata_status strata_window_plan(const strata_moe_desc* desc, int32_t smem_limit, strata_window_info* info) {
+  if (!info) return STRATA_EINVAL;
+  std::memset(info, 0, sizeof(*info));
+  const strata_status st = check_desc(desc);
+  if (st != STRATA_OK) return st;
+  if (smem_limit < 0) return STRATA_EINVAL;
+  const int limit = smem_limit > 0 ? smem_limit : kGb300SmemOptin - kStaticSmemReserve;
+  LayerDev L{};
+  L.d = desc->hidden;
+  L.E = desc->n_experts;
+  L.k = desc->top_k;
+  L.F = desc->ffn;
+  L.Fs = desc->shared_ffn;
+  L.bits = desc->bits;
+  L.renorm = desc->renorm_topk;
+  const KernelCfg C = window_cfg_direct(L, desc->max_rows, limit);
+  if (!C.direct && C.nstages < 2) return STRATA_EUNSUPPORTED;
+  info->stages = C.nstages;
+  info->stage_bytes = C.stage_bytes;
+  info->smem_bytes = C.total_bytes;
+  return STRATA_OK;
+}
+
 strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe_weights* weights, void* cuda_stream,
                                    strata_window** out) {
   if (!out) return STRATA_EINVAL;
@@ -210,7 +239,7 @@ strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe
   W.obuf = reinterpret_cast<float*>(wsb + o_ob);
   W.sbuf = reinterpret_cast<float*>(wsb + o_sb);
 
-  const int limit = optin - 12288;  // leave room for the kernel's static shared memory
+  const int limit = optin - kStaticSmemReserve;
   h->cfg = window_cfg_direct(L, desc->max_rows, limit);
   if (!h->cfg.direct && h->cfg.nstages < 2) {
     free_handle(h);

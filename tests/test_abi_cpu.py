@@ -104,3 +104,73 @@ def test_create_without_gpu_reports_cuda_error(lib):
         pytest.skip("a GPU is present")
     st, h = B.strata_window_create(_desc(), _weights())
     assert st == B.STRATA_ECUDA and h is None
+
+
+# ---- the window-kernel plan a handle would choose (host only) ----
+
+def _plan(spec, monkeypatch=None, env=(), max_rows=8, smem_limit=0):
+    if monkeypatch is not None:
+        for name in ("STRATA_WINDOW_RING", "STRATA_WINDOW_DIRECT"):
+            monkeypatch.delenv(name, raising=False)
+        for name in env:
+            monkeypatch.setenv(name, "1")
+    return B.strata_window_plan(B.desc_of(spec, max_rows), smem_limit)
+
+
+def test_plan_keeps_the_ring_for_the_d2048_layer(lib, monkeypatch):
+    """The d = 2048 4-bit layer keeps a three-stage ring of 40 KB stages."""
+    from slot_decode_window_gb300 import workloads as wlm
+    st, info = _plan(wlm.WORKLOADS["mid"].moe, monkeypatch)
+    assert st == B.STRATA_OK
+    assert (info.stages, info.stage_bytes) == (3, 40960)
+    assert info.smem_bytes <= 232448 - 12288
+    assert info.n_sm == 0 and info.packed_bytes == 0  # fields a plan does not fill
+
+
+@pytest.mark.parametrize("name", ["zipf", "lowbit"])
+def test_plan_streams_the_d4096_layers(lib, monkeypatch, name):
+    """Both 4096-wide layers (4-bit with a ring under three 32 KB stages, and
+    2-bit) take the warp-streamed path: no ring, per-warp FIFOs."""
+    from slot_decode_window_gb300 import workloads as wlm
+    spec = wlm.WORKLOADS[name].moe
+    st, info = _plan(spec, monkeypatch)
+    assert st == B.STRATA_OK and info.stages == 1
+    item = 576 if spec.bits == 4 else 768  # one k-step chunk: codes + scale records
+    assert info.stage_bytes == 16 * 4 * item
+    st, ring = _plan(spec, monkeypatch, env=("STRATA_WINDOW_RING",))
+    assert st == B.STRATA_OK and ring.stages >= 2
+    assert ring.stages * ring.stage_bytes < 96 * 1024  # the short ring the rule avoids
+    assert info.smem_bytes <= ring.smem_bytes
+
+
+def test_plan_overrides_and_shape_rule(lib, monkeypatch):
+    """STRATA_WINDOW_DIRECT forces the streamed path only where every warp gets
+    a k-step of each task; the tiny layer (d = 256: 4 k-steps) stays on the ring."""
+    from slot_decode_window_gb300 import workloads as wlm
+    wide4 = wlm.MoESpec(512, 12, 4, 512, 512, 4, 32)
+    assert _plan(wide4, monkeypatch)[1].stages >= 2
+    assert _plan(wide4, monkeypatch, env=("STRATA_WINDOW_DIRECT",))[1].stages == 1
+    tiny = wlm.WORKLOADS["tiny"].moe
+    assert _plan(tiny, monkeypatch, env=("STRATA_WINDOW_DIRECT",))[1].stages >= 2
+    wide2 = wlm.MoESpec(1024, 12, 4, 1024, 1024, 2, 16)
+    assert _plan(wide2, monkeypatch)[1].stages == 1
+    # both overrides: the ring wins
+    assert _plan(wide2, monkeypatch, env=("STRATA_WINDOW_DIRECT", "STRATA_WINDOW_RING"))[1].stages >= 2
+
+
+def test_plan_limits_and_errors(lib, monkeypatch):
+    from slot_decode_window_gb300 import workloads as wlm
+    mid = wlm.WORKLOADS["mid"].moe
+    for limit in (150_000, 180_000, 220_160):
+        st, info = _plan(mid, monkeypatch, smem_limit=limit)
+        assert st == B.STRATA_OK and info.smem_bytes <= limit
+        # a ring of three or more 32 KB stages, else the warp-streamed path
+        assert info.stages == 1 or (info.stages >= 2 and info.stages * info.stage_bytes >= 96 * 1024)
+    assert _plan(mid, monkeypatch, smem_limit=150_000)[1].stages == 1  # the ring would be short here
+    assert _plan(mid, monkeypatch, smem_limit=220_160)[1].stages == 3
+    assert _plan(mid, monkeypatch, smem_limit=60_000)[0] == B.STRATA_EUNSUPPORTED
+    assert _plan(mid, monkeypatch, smem_limit=-1)[0] == B.STRATA_EINVAL
+    assert B.strata_window_plan(_desc(hidden=0))[0] == B.STRATA_EINVAL
+    assert B.strata_window_plan(_desc(bits=3))[0] == B.STRATA_EUNSUPPORTED
+    assert lib.strata_window_plan(None, 0, ctypes.byref(B.strata_window_info())) == B.STRATA_EINVAL
+    assert lib.strata_window_plan(ctypes.byref(_desc()), 0, None) == B.STRATA_EINVAL
