@@ -211,6 +211,22 @@ def oracle_rows_per_s(wl, layer_np, xs, budget_s, per_row=True):
 # reference arm: the oracle
 
 
+def reduce_max_over_ranks(v: float, world: int, device) -> float:
+    """The largest of v over all ranks (the slowest rank's time); v itself on one rank."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, seconds_max: float) -> float:
+    """Units all ranks processed over the slowest rank's time (weak scaling)."""
+    return units_per_rank * world / seconds_max
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -353,11 +369,7 @@ def run_ours(args, rank, world, local_rank):
         return ms, nbytes, wall
 
     def reduce_max(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max_over_ranks(v, world, dev)
 
     gpu_id = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
     gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else str(gpu_id or local_rank)
@@ -367,8 +379,7 @@ def run_ours(args, rank, world, local_rank):
     T = args.rows
     ms, nbytes, wall = timed(T, args.steps, max(3, args.warmup))
     total_s = reduce_max(sum(ms) / 1e3)
-    rows_total = args.steps * T * world
-    value = rows_total / total_s
+    value = whole_job_rate(args.steps * T, world, total_s)
 
     # sweep
     sweep = {}
