@@ -454,7 +454,7 @@ def run_ours(args, rank, world, local_rank):
         evs.append((a, b))
     torch.cuda.synchronize()
     e2e_s = reduce_max(sum(a.elapsed_time(b) for a, b in evs) / 1e3)
-    e2e = {"value": e2e_steps * T * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": T * d * 4,
+    e2e = {"value": whole_job_rate(e2e_steps * T, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": T * d * 4,
            "d2h_bytes_per_step": T * d * 4}
 
     workloads = None
