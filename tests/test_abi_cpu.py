@@ -174,3 +174,18 @@ def test_plan_limits_and_errors(lib, monkeypatch):
     assert B.strata_window_plan(_desc(bits=3))[0] == B.STRATA_EUNSUPPORTED
     assert lib.strata_window_plan(None, 0, ctypes.byref(B.strata_window_info())) == B.STRATA_EINVAL
     assert lib.strata_window_plan(ctypes.byref(_desc()), 0, None) == B.STRATA_EINVAL
+
+
+@pytest.mark.parametrize("ffn,shared_ffn", [(256, 0), (1024, 256), (1024, 448)])
+def test_plan_keeps_the_ring_when_a_warp_would_get_no_k_step(lib, monkeypatch, ffn, shared_ffn):
+    """A d = 4096 4-bit layer leaves a short ring, but the warp-streamed path
+    needs at least 8 64-column k-steps in every task (each warp of a sub-tile
+    must get one): an expert or shared width under 512 keeps the ring."""
+    from slot_decode_window_gb300 import workloads as wlm
+    spec = wlm.MoESpec(4096, 16, 2, ffn, shared_ffn, 4, 32)
+    st, info = _plan(spec, monkeypatch)
+    assert st == B.STRATA_OK and info.stages >= 2
+    st, forced = _plan(spec, monkeypatch, env=("STRATA_WINDOW_DIRECT",))
+    assert st == B.STRATA_OK and forced.stages >= 2
+    wide = wlm.MoESpec(4096, 16, 2, 1024, 512, 4, 32)
+    assert _plan(wide, monkeypatch)[1].stages == 1
