@@ -10,8 +10,9 @@
 //
 // One launch per window, one CTA per SM (cooperative launch, so all CTAs are
 // resident and the few cross-CTA waits below always end):
-//   R. router: every warp takes (expert, 256-column chunk) pairs of the fp32
-//      router GEMV and writes partial logits; all threads turn x into the
+//   R. router: each CTA stages one 512-column chunk of the rows of x and its
+//      warps take that chunk's experts of the fp32 router GEMV, writing
+//      partial logits; the CTA then turns its share of the chunk into the
 //      activation fragments of the gate/up MMAs.  One grid barrier follows.
 //   P. every CTA sums the partial logits in a fixed order and derives the same
 //      routing plan: fp32 softmax, top-k by logit (ties to the lower expert),
