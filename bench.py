@@ -47,7 +47,6 @@ def parse():
     p.add_argument("--workload", default="mid")
     p.add_argument("--rows", type=int, default=8)
     p.add_argument("--sweep-steps", type=int, default=500)
-    p.add_argument("--cpu-seconds", type=float, default=20.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-stack", action="store_true", help="skip the 48-layer stack measurement")
     p.add_argument("--no-workloads", action="store_true", help="skip the zipf and lowbit layer measurements")
@@ -56,6 +55,13 @@ def parse():
     p.add_argument("--mode", choices=("full", "windows", "stack"), default="full",
                    help="windows: only warmup + K windows at --rows (a clean launch sequence for ncu)")
     return p.parse_args()
+
+
+def bench_config(wl, T, world):
+    """The workload keys of the JSON line, identical for both arms."""
+    return {"workload": workload_desc(wl, T), "T": T, "windows": N_WINDOWS,
+            "l2": "flushed before every timed window (memset of 2x L2 outside the events)",
+            "parallelism": "replicas only" if world > 1 else "1 GPU"}
 
 
 def workload_desc(wl, T):
@@ -187,24 +193,87 @@ def cpu_threads():
     return os.cpu_count() or 1
 
 
-def oracle_rows_per_s(wl, layer_np, xs, budget_s, per_row=True):
-    """Time the fp64 oracle on rows of the windows until the budget is spent."""
+def percentiles(vals):
+    """(p10, median, p90) of a list, by linear interpolation between order statistics."""
+    v = sorted(vals)
+
+    def q(f):
+        i = f * (len(v) - 1)
+        lo = int(i)
+        hi = min(lo + 1, len(v) - 1)
+        return v[lo] + (v[hi] - v[lo]) * (i - lo)
+    return q(0.1), q(0.5), q(0.9)
+
+
+def oracle_subset(layer_np, xs):
+    """The oracle's view of a layer holding only the routed experts the rows of
+    the windows ``xs`` select (matrix stacks as {expert: array}), so that the
+    child process that times the oracle receives a few hundred MB at most."""
     import oracle
-    done = 0
-    t0 = time.perf_counter()
-    w = 0
-    while True:
-        x = xs[w % len(xs)]
+    need = set()
+    for x in xs:
         for t in range(x.shape[0]):
-            oracle.moe_window(x[t:t + 1], layer_np)
-            done += 1
-            if time.perf_counter() - t0 >= budget_s:
-                break
-        w += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    el = time.perf_counter() - t0
-    return done / el, done, el
+            need.update(int(e) for e in oracle.router(x[t], layer_np.router_w, layer_np.router_b,
+                                                      layer_np.top_k, layer_np.renorm)[2])
+
+    def sub(q):
+        return oracle.OQMat({e: q.codes[e] for e in need}, {e: q.scale[e] for e in need},
+                            {e: q.min[e] for e in need}, q.rows, q.cols, q.bits, q.block)
+    import dataclasses
+    return dataclasses.replace(layer_np, gate=sub(layer_np.gate), up=sub(layer_np.up), down=sub(layer_np.down))
+
+
+def _time_oracle_child(job):
+    """Runs in a spawned child: the fp64 oracle over whole windows; (seconds, rows)."""
+    import oracle
+    kind, payload, xs = job
+    t0 = time.perf_counter()
+    rows = 0
+    for x in xs:
+        if kind == "moe":
+            oracle.moe_window(x, payload)
+        else:  # one decoder layer, row by row
+            dense, moe = payload
+            for t in range(x.shape[0]):
+                oracle.decoder_layer_row(x[t], dense, moe)
+        rows += x.shape[0]
+    return time.perf_counter() - t0, rows
+
+
+def time_oracle(kind, payload, xs, threads):
+    """The oracle timed in a fresh spawned process whose BLAS uses ``threads``
+    threads (set through the environment before numpy loads in the child)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    names = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+    old = {n: os.environ.get(n) for n in names}
+    for n in names:
+        os.environ[n] = str(threads)
+    try:
+        with cf.ProcessPoolExecutor(1, mp_context=mp.get_context("spawn")) as ex:
+            sec, rows = ex.submit(_time_oracle_child, (kind, payload, xs)).result()
+    finally:
+        for n, v in old.items():
+            if v is None:
+                os.environ.pop(n, None)
+            else:
+                os.environ[n] = v
+    return sec, rows
+
+
+def cpu_baselines(jobs):
+    """Each job (name, kind, payload, windows, T): the oracle with all host
+    cores and with one, rows/s and windows/s."""
+    out = {}
+    cores = os.cpu_count() or 1
+    for name, kind, payload, xs, T in jobs:
+        entry = {"T": T, "windows": len(xs), "kind": "oracle"}
+        for label, th in (("all_cores", cores), ("one_thread", 1)):
+            sec, rows = time_oracle(kind, payload, xs, th)
+            entry[label] = {"threads": th, "seconds": sec, "rows_per_s": rows / sec,
+                            "windows_per_s": len(xs) / sec}
+        out[name] = entry
+    return out
 
 
 # ---------------------------------------------------------------------------------------------
@@ -255,8 +324,8 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(wl, T), "step": "one row of a T-row window, evaluated on its own",
-                   "parallelism": "host cores (numpy BLAS)"},
+        "config": bench_config(wl, T, world),
+        "step": "one row of a T-row window, evaluated on its own by the fp64 oracle on the host cores (numpy BLAS)",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{args.steps} rows cycled over 8 seeded windows of T={T}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -386,8 +455,11 @@ def run_ours(args, rank, world, local_rank):
     for Ts_ in SWEEP:
         m, b, _ = timed(Ts_, args.sweep_steps, 10)
         tot = sum(m) / 1e3
+        q10, q50, q90 = percentiles(m)
         sweep[str(Ts_)] = {"rows_per_s": args.sweep_steps * Ts_ / tot, "windows_per_s": args.sweep_steps / tot,
-                           "us_per_window_median": 1e3 * statistics.median(m),
+                           "us_per_window_mean": 1e6 * tot / args.sweep_steps,
+                           "us_per_window_p10": 1e3 * q10, "us_per_window_median": 1e3 * q50,
+                           "us_per_window_p90": 1e3 * q90,
                            "algorithmic_GBps": b / tot / 1e9,
                            "mean_distinct_experts": sum(nd[Ts_]) / len(nd[Ts_])}
 
@@ -457,37 +529,46 @@ def run_ours(args, rank, world, local_rank):
     e2e = {"value": whole_job_rate(e2e_steps * T, world, e2e_s), "unit": UNIT, "h2d_bytes_per_step": T * d * 4,
            "d2h_bytes_per_step": T * d * 4}
 
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    cpu_jobs = []
+    if want_cpu:
+        from tests.helpers import omoe
+        xs = [X[T][w].cpu().numpy() for w in range(8)]
+        cpu_jobs.append((args.workload, "moe", oracle_subset(omoe(layer), xs), xs, T))
     workloads = None
     if not args.no_workloads:
-        workloads = {"zipf": measure_workload("zipf", (8,), dev, flush, stream, peak),
-                     "lowbit": measure_workload("lowbit", (1, 8), dev, flush, stream, peak)}
-    stack = None if args.no_stack else measure_stack(args, dev, flush, stream, peak)
+        workloads = {"zipf": measure_workload("zipf", (8,), dev, flush, stream, peak, cpu_jobs if want_cpu else None),
+                     "lowbit": measure_workload("lowbit", (1, 2, 4, 8), dev, flush, stream, peak,
+                                                cpu_jobs if want_cpu else None)}
+    stack = None if args.no_stack else measure_stack(args, dev, flush, stream, peak, cpu_jobs if want_cpu else None)
     clocks = sampler.stop()
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        from tests.helpers import omoe
-        ol = omoe(layer)
-        xs = [X[T][w].cpu().numpy() for w in range(4)]
-        rps, done, el = oracle_rows_per_s(wl, ol, xs, args.cpu_seconds)
-        cpu = {"value": rps, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-               "sample": f"{done} rows of T={T} windows, each evaluated on its own by the fp64 oracle, {el:.1f} s"}
+    cpu = cpu_all = None
+    if want_cpu:
+        cpu_all = cpu_baselines(cpu_jobs)
+        head = cpu_all[args.workload]
+        cpu = {"value": head["all_cores"]["rows_per_s"], "unit": UNIT, "cores": head["all_cores"]["threads"],
+               "kind": "oracle",
+               "sample": f"{head['windows']} windows of T={T} of the bench's inputs, each window evaluated row by "
+                         f"row by the fp64 oracle in a spawned process with {head['all_cores']['threads']} BLAS "
+                         f"threads, {head['all_cores']['seconds']:.1f} s",
+               "one_thread": head["one_thread"]}
+    p10, p50, p90 = percentiles(ms)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": workload_desc(wl, T), "T": T, "windows": N_WINDOWS,
-                       "l2": "flushed before every timed window (memset of 2x L2 outside the events)",
-                       "parallelism": "replicas only" if world > 1 else "1 GPU",
-                       "arith": "codes -> exact fp16 integers; mma.sync f16 x (fp16 hi + lo activations), fp32 "
-                                "accumulate; fp32 router, softmax, SwiGLU, combine"},
+            "config": bench_config(wl, T, world),
+            "arith": "codes -> exact fp16 integers; mma.sync f16 x (fp16 hi + lo activations), fp32 accumulate; "
+                     "fp32 router, softmax, SwiGLU, combine",
             "roofline": roofline, "sweep": sweep, "graph": graph, "workloads": workloads, "stack48": stack, "e2e": e2e,
             "clocks": clocks,
-            "cpu_baseline": cpu,
+            "cpu_baseline": cpu, "cpu_baselines": cpu_all,
             "gpu_launches": args.steps,
-            "window_us_median": 1e3 * statistics.median(ms), "wall_s_timed_region": wall,
+            "window_us": {"mean": 1e3 * statistics.mean(ms), "p10": 1e3 * p10, "median": 1e3 * p50, "p90": 1e3 * p90},
+            "rows_per_s_at_median": T / (p50 / 1e3), "wall_s_timed_region": wall,
             "handle": {"n_sm": info.n_sm, "stages": info.stages, "stage_bytes": info.stage_bytes,
                        "smem_bytes": info.smem_bytes},
         }
@@ -495,16 +576,22 @@ def run_ours(args, rank, world, local_rank):
     win.close()
 
 
-def measure_workload(name, Ts, dev, flush, stream, peak, steps=300):
+def measure_workload(name, Ts, dev, flush, stream, peak, cpu_jobs=None, steps=300):
     """Another layer shape of the pages' workloads at the given row counts:
     mean kernel time per window (profiling-mode events around the launch, L2
-    flushed before each window) over its algorithmic bytes."""
+    flushed before each window) over its algorithmic bytes.  With cpu_jobs, a
+    job timing the oracle on three T = max(Ts) windows of this layer is added."""
     import numpy as np
     import torch
     from slot_decode_window_gb300 import binding, workloads as wlm
     wl = wlm.WORKLOADS[name]
     layer = wlm.make_moe_layer(wl.moe, seed=0, cfg_id=wl.cfg_id, device=str(dev))
     win = binding.Window(layer, max_rows=8)
+    if cpu_jobs is not None:
+        from tests.helpers import omoe_lazy
+        Tc = max(Ts)
+        xs = [wlm.make_window(wl, Tc, seed=0, window=2000 * Tc + w) for w in range(3)]
+        cpu_jobs.append((name, "moe", oracle_subset(omoe_lazy(layer), xs), xs, Tc))
     del layer
     torch.cuda.empty_cache()
     info = win.info()
@@ -532,7 +619,10 @@ def measure_workload(name, Ts, dev, flush, stream, peak, steps=300):
         win.sync()
         tot = sum(ms) / 1e3
         achieved = nbytes / tot / 1e9
-        out[str(T)] = {"us_per_window_mean": 1e6 * tot / steps, "rows_per_s": steps * T / tot,
+        q10, q50, q90 = percentiles(ms)
+        out[str(T)] = {"us_per_window_mean": 1e6 * tot / steps, "us_per_window_p10": 1e3 * q10,
+                       "us_per_window_median": 1e3 * q50, "us_per_window_p90": 1e3 * q90,
+                       "rows_per_s": steps * T / tot,
                        "windows_per_s": steps / tot, "algorithmic_MB_per_window": nbytes / steps / 1e6,
                        "mean_distinct_experts": sum(nd) / len(nd), "achieved_GBps": achieved,
                        "frac_of_measured_hbm": achieved / peak}
@@ -540,15 +630,21 @@ def measure_workload(name, Ts, dev, flush, stream, peak, steps=300):
     return out
 
 
-def measure_stack(args, dev, flush, stream, peak):
+def measure_stack(args, dev, flush, stream, peak, cpu_jobs=None):
     """The 48-layer decoder stack (dense 4-bit q/k/v/o + the mid MoE per layer),
-    T = 8, one launch per window, L2 flushed before each window."""
+    T = 8, one launch per window, L2 flushed before each window.  With
+    cpu_jobs, a job timing the oracle on one window through one layer (the
+    stack's per-layer cost; a window through all layers is 48 of these) is added."""
     import numpy as np
     import torch
     from slot_decode_window_gb300 import binding, workloads as wlm
     wl = wlm.WORKLOADS["stack48"]
     moe = [wlm.make_moe_layer(wl.moe, seed=0, cfg_id=wl.cfg_id, layer=l, device=str(dev)) for l in range(wl.n_layers)]
     dense = [wlm.make_dense_layer(wl, seed=0, layer=l, device=str(dev)) for l in range(wl.n_layers)]
+    if cpu_jobs is not None:
+        from tests.helpers import odense, omoe
+        cpu_jobs.append(("stack48_one_layer", "layer", (odense(dense[0], wl), omoe(moe[0])),
+                         [wlm.make_window(wl, 8, seed=0, window=0)], 8))
     stk = binding.Stack(wl, moe, dense, max_rows=8)
     del moe, dense
     torch.cuda.empty_cache()

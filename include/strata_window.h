@@ -126,6 +126,13 @@ typedef struct {
  * STRATA_WINDOW_DIRECT (any value) forces the warp-streamed path where the
  * shape allows it (every warp gets a k-step of each task).  Results of the two
  * paths agree within the output tolerance, not bit for bit.
+ * Two more variables, also read here, bound the device's waits:
+ * STRATA_WAIT_CYCLES (an integer from 1000 to 2^40; default 2^31, about a
+ * second at GB300 clocks) is the limit of every bounded wait of the kernel,
+ * in SM clock cycles; STRATA_TEST_BARRIER_EXTRA (default 0) makes every grid
+ * barrier wait for that many arrivals that never come.  They exist so that
+ * failure tests can make a wait run out: each CTA then gives up after the
+ * limit, records EDEVICE and returns.  Malformed values are ignored.
  * Returns EINVAL (bad pointer or shape), EUNSUPPORTED (bits/block pair or size
  * limits), ENOMEM, ECUDA. */
 strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe_weights* weights,
@@ -167,7 +174,9 @@ strata_status strata_moe_window_forward_graph(strata_window* h, const float* x, 
                                               void* cuda_stream);
 
 /* Wait for the handle's last forward call to finish; report (and clear) any
- * error the GPU recorded: EDEVICE in that case. */
+ * error the GPU recorded: EDEVICE in that case.  After an error the handle's
+ * grid-barrier count is reset too (a window that gave up part way may have
+ * left it off a multiple of the grid), so the next window starts clean. */
 strata_status strata_window_sync(strata_window* h);
 
 /* Fill *info with the sizes the handle chose. */

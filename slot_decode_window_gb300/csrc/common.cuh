@@ -113,6 +113,8 @@ struct WindowBufs {
   float* partial;          // router partial logits [njb][kMaxRows][E]
   int njb;                 // column chunks of the router GEMV
   unsigned* err;
+  long long wait_cycles;   // limit of every bounded device wait, in SM clock cycles
+  int bar_extra;           // arrivals a grid barrier expects beyond the grid (0; > 0 only in failure tests)
   // decoder-layer extras (stack kernel only; null in the single-layer kernel)
   const float* rinv;       // [T] 1 / RMS of each row of x (inputs are x * rinv)
   const float* resid;      // [T][d] added to y in the combine

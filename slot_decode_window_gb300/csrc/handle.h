@@ -36,4 +36,6 @@ struct strata_window {
 namespace strata {
 // The STRATA_FAULT test hook: true when the environment names `what`.
 bool fault_is(const char* what);
+// An integer from the environment, or dflt when unset, malformed or outside [lo, hi].
+long long env_int(const char* name, long long dflt, long long lo, long long hi);
 }  // namespace strata

@@ -239,7 +239,11 @@ strata_status strata_stack_sync(strata_stack* s) {
     return STRATA_ECUDA;
   }
   if (err != 0) {
+    // as strata_window_sync: the failed window's grid-barrier count restarts at zero
     cudaMemset(s->W.err, 0, sizeof(unsigned));
+    cudaMemset(s->W.gbar, 0, sizeof(unsigned long long));
+    cudaDeviceSynchronize();
+    cudaGetLastError();
     return STRATA_EDEVICE;
   }
   return STRATA_OK;

@@ -18,6 +18,15 @@ bool strata::fault_is(const char* what) {
   return f && std::strcmp(f, what) == 0;
 }
 
+long long strata::env_int(const char* name, long long dflt, long long lo, long long hi) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  char* end = nullptr;
+  const long long n = std::strtoll(v, &end, 10);
+  if (*end != '\0' || n < lo || n > hi) return dflt;
+  return n;
+}
+
 namespace {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -231,6 +240,11 @@ strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe
   h->partial = reinterpret_cast<float*>(wsb + o_part);
   W.partial = h->partial;
   W.njb = njb;
+  // bounded device waits: 2^31 cycles (about a second) unless a diagnostic
+  // override asks for a shorter limit; no extra grid-barrier arrivals unless a
+  // failure test asks for some
+  W.wait_cycles = env_int("STRATA_WAIT_CYCLES", 1LL << 31, 1000, 1LL << 40);
+  W.bar_extra = (int)env_int("STRATA_TEST_BARRIER_EXTRA", 0, 0, 1 << 20);
   W.xfrag = reinterpret_cast<__half*>(wsb + o_xf);
   W.hfrag = reinterpret_cast<__half*>(wsb + o_hf);
   W.hsum = reinterpret_cast<float*>(wsb + o_hs);
@@ -376,7 +390,13 @@ strata_status strata_window_sync(strata_window* h) {
     return STRATA_ECUDA;
   }
   if (err != 0) {
+    // the window that failed may have left its grid-barrier count off a
+    // multiple of the grid (CTAs that gave up before others arrived): start
+    // the next window from zero
     cudaMemset(h->W.err, 0, sizeof(unsigned));
+    cudaMemset(h->W.gbar, 0, sizeof(unsigned long long));
+    cudaDeviceSynchronize();
+    cudaGetLastError();
     return STRATA_EDEVICE;
   }
   return STRATA_OK;

@@ -49,7 +49,6 @@ namespace {
 
 constexpr int kMaxSub = 4;  // sub-tiles per task
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr long long kWaitCycles = 1LL << 31;  // about a second at GB300 clocks
 
 // Stage timestamps for timing builds (-DSTRATA_STAMPS): one lane of the CTA
 // records %globaltimer at stage boundaries into g_stamps[cta][slot].  The
@@ -97,7 +96,10 @@ __device__ __forceinline__ void trace(int phase, int slot, int ev) {
   } while (0)
 #endif
 
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigned* err, volatile int* abort_flag) {
+// Every wait below is bounded by W.wait_cycles (by default 2^31 cycles, about
+// a second at GB300 clocks); one that gives up sets the error word and returns.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigned* err, volatile int* abort_flag,
+                                         long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
@@ -105,7 +107,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, unsigne
 #pragma unroll 1
     for (int i = 0; i < 8; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       atomicOr(err, kErrTimeout);
       *abort_flag = 1;
       return false;
@@ -512,18 +514,19 @@ __device__ __noinline__ void router_stage(const LayerDev& L, const WindowBufs& W
 }
 
 // All CTAs arrive; thread 0 waits (bounded) until every CTA of this window has.
-// The counter only grows: the window's target is the next multiple of the grid.
+// The counter only grows: the window's target is the next multiple of the grid
+// (plus W.bar_extra, which is 0 except in tests that make the wait run out).
 __device__ bool grid_barrier(const WindowBufs& W, int* s_ok) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     const unsigned long long n = gridDim.x;
     const unsigned long long old = atomicAdd(W.gbar, 1ull);
-    const unsigned long long target = (old / n + 1) * n;
+    const unsigned long long target = (old / n + 1) * n + (unsigned long long)W.bar_extra;
     const long long t0 = clock64();
     int ok = 1;
     while (ld_acquire_u64(W.gbar) < target) {
-      if (clock64() - t0 > kWaitCycles) {
+      if (clock64() - t0 > W.wait_cycles) {
         atomicOr(W.err, kErrTimeout);
         ok = 0;
         break;
@@ -1025,7 +1028,8 @@ __device__ bool produce(const LayerDev& L, const WindowBufs& W, const KernelCfg&
       const int ks0 = P.cks[kv][ch], ks1 = P.cks[kv][ch + 1];
       const int mk0 = P.cmk[kv][ch], mk1 = P.cmk[kv][ch + 1];
       const int stage = rp.stage;
-      if (rp.n >= C.nstages && !wait_bar(&rg.empty[stage], rp.parity ^ 1u, W.err, rg.abort_flag)) return false;
+      if (rp.n >= C.nstages && !wait_bar(&rg.empty[stage], rp.parity ^ 1u, W.err, rg.abort_flag, W.wait_cycles))
+        return false;
       if (PHASE < 2) PTRACE(PHASE, (task - pt.t0) * P.nchunks + ch);
       const uint32_t cbytes = (uint32_t)((ks1 - ks0) * Fmt<BITS>::kChunk), mbytes = (uint32_t)((mk1 - mk0) * 512);
       uint8_t* dst = rg.base + (size_t)stage * C.stage_bytes;
@@ -1111,7 +1115,7 @@ __device__ __forceinline__ void enter_group(const LayerDev& L, const WindowBufs&
       const int need = tk.shared ? sp.pt[0].ntask_s : sp.pt[0].ntask_e;
       const long long t0 = clock64();
       while (!*abort_flag && ld_acquire(W.done_gu + tk.group) < need) {
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > W.wait_cycles) {
           atomicOr(W.err, kErrTimeout);
           *abort_flag = 1;
           break;
@@ -1257,7 +1261,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
       const int k0 = (kg * nk) / kWPS, k1 = ((kg + 1) * nk) / kWPS;
       const int m0 = (kg * nm) / kWPS, m1 = ((kg + 1) * nm) / kWPS;
       const int stage = rp.stage;
-      if (wait_bar(&rg.full[stage], rp.parity, W.err, rg.abort_flag)) {
+      if (wait_bar(&rg.full[stage], rp.parity, W.err, rg.abort_flag, W.wait_cycles)) {
         if (PHASE < 2 && ch == 0) TRACE(0, PHASE, task - pt.t0, 1);
         const uint8_t* st = rg.base + (size_t)stage * C.stage_bytes + sub * P.sub_stride;
         constexpr bool kVmap = PHASE == 3;
@@ -1334,7 +1338,8 @@ __device__ __forceinline__ int task_k(const LayerDev& L, const Task& tk) {
 
 // The copying side of a warp's item stream over its CTA's task range of one
 // phase.  Every warp has at least one item in every task (the kernel is used
-// only when each warp's k-range is non-empty).
+// only when each warp's k-range is non-empty); `set` checks this and, should
+// it fail, flags the error word and stops the stream.
 template <int BITS, int PHASE, int NS>
 struct DStream {
   static constexpr int kMT = PHASE == 0 ? NS / 2 : NS;
@@ -1354,6 +1359,15 @@ struct DStream {
     }
     const int K = task_k<PHASE>(L, tk);
     const ItemRange r = item_range<BITS, NS>(K, kg);
+    if (r.n < 1) {
+      // a warp with no item in this task would never reach the item that
+      // moves its stream on, and would copy past the task's tile: stop
+      // copying instead (the host's shape rule rules this out)
+      atomicOr(err, kErrConfig);
+      *abort_flag = 1;
+      task = t1;
+      return;
+    }
     const int nks = K / Fmt<BITS>::kKstep, nmk = (K / Fmt<BITS>::kBlock + 15) / 16;
     const int tbytes = nks * Fmt<BITS>::kChunk + nmk * 512;
     const MatRef M = task_mat<PHASE, kMT>(L, tk.shared, sub);
@@ -1613,12 +1627,12 @@ __device__ __noinline__ void combine_all(const LayerDev& L, const WindowBufs& W)
 
 // The producer thread's drain after an abort: every copy it issued lands
 // before the CTA may move on or exit.
-__device__ __noinline__ void drain_ring(const Ring& rg, const KernelCfg& C, const RingPos& rp) {
+__device__ __noinline__ void drain_ring(const Ring& rg, const KernelCfg& C, const RingPos& rp, long long limit) {
   const int it = rp.n;
   for (int j = (it > C.nstages ? it - C.nstages : 0); j < it; ++j) {
     const long long tw = clock64();
     while (!mbar_try_wait(&rg.full[j % C.nstages], (j / C.nstages) & 1)) {
-      if (clock64() - tw > kWaitCycles) break;
+      if (clock64() - tw > limit) break;
     }
   }
 }
@@ -1734,7 +1748,7 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
         else produce<BITS, 1, 1>(L, W, C, sp, rg, rp);
       }
       STAMP(kConsumerThreads, 12);
-      if (*rg.abort_flag) drain_ring(rg, C, rp);
+      if (*rg.abort_flag) drain_ring(rg, C, rp, W.wait_cycles);
     }
     return true;
   }
@@ -1784,7 +1798,7 @@ __device__ __forceinline__ void dense_phase(const LayerDev& L, const WindowBufs&
       if (ns == 4) produce<BITS, PHASE, 4>(L, W, C, sp, rg, rp);
       else if (ns == 2) produce<BITS, PHASE, 2>(L, W, C, sp, rg, rp);
       else produce<BITS, PHASE, 1>(L, W, C, sp, rg, rp);
-      if (*rg.abort_flag) drain_ring(rg, C, rp);
+      if (*rg.abort_flag) drain_ring(rg, C, rp, W.wait_cycles);
     }
     return;
   }

@@ -112,31 +112,48 @@ def test_stack48_shapes_three_layers_all_rows():
     stk.close()
 
 
-def test_stack48_full_depth_sampled_row_and_determinism():
-    """All 48 layers, T = 8 (the full workload): one sampled row whose fp64 margin
-    holds at every layer is checked against the oracle; the run repeats bit for bit."""
+class _Fixed:
+    """Trajectories computed beforehand, looked up by row."""
+
+    def __init__(self, x, trajs):
+        self.memo = {x[t].tobytes(): trajs[t] for t in range(x.shape[0])}
+
+    def get(self, row):
+        return self.memo[row.tobytes()]
+
+
+def test_stack48_full_depth_rows_and_determinism():
+    """All 48 layers, T = 8 (the full workload).  Every row of a window whose
+    fp64 router margin holds at every layer (about 0.983^48 = 44% of rows) is
+    checked against the oracle, over windows until at least three rows have
+    been; the run repeats bit for bit."""
     from slot_decode_window_gb300.binding import Stack
+    from tests import oracle_lean
     wl = wlm.WORKLOADS["stack48"]
     moe, dense = _layers(wl, wl.n_layers)
     stk = Stack(wl, moe, dense, max_rows=8)
-    x = wlm.make_window(wl, 8, seed=0, window=0)
-    xt = torch.from_numpy(x).cuda()
-    y1, res = stk.forward(xt, outputs=True)
-    y2 = stk.forward(xt)
-    stk.sync()
-    y1n, y2n = y1.cpu().numpy(), y2.cpu().numpy()
-    np.testing.assert_array_equal(y1n, y2n)
-    assert np.isfinite(y1n).all()
-    idx = res["topk_idx"].cpu().numpy()
-    assert idx.min() >= 0 and idx.max() < wl.moe.n_experts
-    nd = res["n_distinct"].cpu().numpy()
-    assert (nd >= wl.moe.top_k).all() and (nd <= 8 * wl.moe.top_k).all()
-    traj = _Traj([odense(dl, wl) for dl in dense], [omoe_lazy(m) for m in moe])
+    dense_o, moe_o = [odense(dl, wl) for dl in dense], [omoe_lazy(m) for m in moe]
     checked = 0
-    for t in range(3):
-        if traj(x[t]):
-            _compare(res, y1n.astype(np.float64), x, traj, [t], wl.n_layers)
-            checked += 1
-            break
-    assert checked == 1, "no sampled row kept a 1e-3 margin at every layer"
+    with oracle_lean.spawn_pool() as pool:
+        for window in range(4):
+            x = wlm.make_window(wl, 8, seed=0, window=window)
+            xt = torch.from_numpy(x).cuda()
+            y1, res = stk.forward(xt, outputs=True)
+            y2 = stk.forward(xt)
+            stk.sync()
+            y1n, y2n = y1.cpu().numpy(), y2.cpu().numpy()
+            np.testing.assert_array_equal(y1n, y2n)
+            assert np.isfinite(y1n).all()
+            idx = res["topk_idx"].cpu().numpy()
+            assert idx.min() >= 0 and idx.max() < wl.moe.n_experts
+            nd = res["n_distinct"].cpu().numpy()
+            assert (nd >= wl.moe.top_k).all() and (nd <= 8 * wl.moe.top_k).all()
+            trajs = oracle_lean.stack_rows(x, dense_o, moe_o, pool=pool)
+            rows = [t for t in range(8) if trajs[t][4] >= MARGIN]
+            if rows:
+                _compare(res, y1n.astype(np.float64), x, _Fixed(x, trajs), rows, wl.n_layers)
+                checked += len(rows)
+            if checked >= 3:
+                break
+    assert checked >= 3, f"only {checked} rows kept a 1e-3 margin at every layer"
     stk.close()
