@@ -781,6 +781,25 @@ __device__ __forceinline__ void split_tasks(const WindowBufs& W, SPlan& sp, bool
   __syncwarp();
 }
 
+// Zero the sum slots of blocks nb .. 16 nmk - 1 (past the end of a K of nb
+// blocks) in every column of a group of R rows (paired: 2R columns of one
+// set; else R columns of both sets).
+__device__ __forceinline__ void zero_padded_sums(__half* bs, const KernelCfg& C, int nb, int nmk, int R, bool paired,
+                                                 int ctid) {
+  const int npad = nmk * 16 - nb;
+  if (npad <= 0) return;
+  const int ncols = paired ? 2 * R : R;
+  const __half z = __float2half_rn(0.f);
+  for (int i = ctid; i < ncols * npad; i += kConsumerThreads) {
+    const int col = i / npad, blk = nb + (i - col * npad);
+    const int spos = frag_sum_pos(blk);
+    const int mk = spos >> 4, c = (spos >> 2) & 3, slot = spos & 3;
+    const int o = mk * 128 + col * 16 + c * 4 + slot;
+    bs[o] = z;
+    if (!paired) bs[C.bsum_halves + o] = z;
+  }
+}
+
 // Stage one group's activations into shared memory (all consumer threads).
 // Phases 0 and 2: copy x fragments (written by stage R or D0).  Phase 1: copy
 // h fragments (written by the gate/up epilogue) and form the block sums from
@@ -821,6 +840,11 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
                  row_base(r) + (long long)part * K + ks * 4 * S + c * S + p * 8);
     }
     if constexpr (PHASE == 1) {
+      // padded block slots of the last min group (blocks K/B .. 16 nmk - 1):
+      // their min fragments are zero, but an earlier group may have left a
+      // non-finite sum there (0 x NaN = NaN), so they are cleared for every
+      // column this group uses
+      zero_padded_sums(bs, C, K / B, nmk, R, paired, ctid);
       // block sums from the 16-element partial sums, split into hi/lo
       constexpr int kParts = B / 16;
       for (int i = ctid; i < R * (K / B); i += kConsumerThreads) {
@@ -858,6 +882,7 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
     }
     cp_async_wait_all();
   } else {
+    zero_padded_sums(bs, C, L.dq / B, (L.dq / B + 15) / 16, R, paired, ctid);
     // v (K = dkv): one element per thread and step; a warp covers 32
     // consecutive elements of one row (K is a multiple of 64), so block sums
     // come from lane shuffles, written for every block of the broadcast input
