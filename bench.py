@@ -503,6 +503,9 @@ def run_ours(args, rank, world, local_rank):
                 "traffic": traffic, "algorithmic_bytes_per_launch": wb / prof_steps,
                 "kernel_us_mean": 1e3 * statistics.mean(k_ms), "kernel_us_median": 1e3 * statistics.median(k_ms)}
 
+    # the adaptive tier's bookkeeping attached (counters every window, a round every 4)
+    tier = measure_tier(win, X[T], Y[:T], T, flush, min(args.steps, 300))
+
     # end to end through host buffers
     xh = torch.empty(N_WINDOWS, T, d, dtype=torch.float32).pin_memory()
     xh.copy_(X[T].cpu())
@@ -563,7 +566,8 @@ def run_ours(args, rank, world, local_rank):
             "config": bench_config(wl, T, world),
             "arith": "codes -> exact fp16 integers; mma.sync f16 x (fp16 hi + lo activations), fp32 accumulate; "
                      "fp32 router, softmax, SwiGLU, combine",
-            "roofline": roofline, "sweep": sweep, "graph": graph, "workloads": workloads, "stack48": stack, "e2e": e2e,
+            "roofline": roofline, "sweep": sweep, "graph": graph, "tier": tier, "workloads": workloads,
+            "stack48": stack, "e2e": e2e,
             "clocks": clocks,
             "cpu_baseline": cpu, "cpu_baselines": cpu_all,
             "gpu_launches": args.steps,
@@ -574,6 +578,38 @@ def run_ours(args, rank, world, local_rank):
         }
         print(json.dumps(line), flush=True)
     win.close()
+
+
+def measure_tier(win, X, Y, T, flush, steps):
+    """Window kernel time with an adaptive tier attached (capacity E/2, a round
+    every 4 windows, up to 8 swaps, decay 0.5, min gain 1.5) against the same
+    windows without one, profiling-mode events around the launch."""
+    from slot_decode_window_gb300 import binding as B
+    E = win.spec.n_experts
+    st, tier = B.strata_tier_create(B.strata_tier_desc(E, max(1, E // 2), 4, 8, 0.5, 1.5))
+    B.check(st, "strata_tier_create")
+    out = {}
+    try:
+        for label, t in (("without", None), ("with", tier)):
+            B.check(B.strata_window_set_tier(win.handle, t), "strata_window_set_tier")
+            win.set_profiling(True)
+            ms = []
+            for i in range(steps):
+                flush_and_hold(flush)
+                win.forward(X[i % N_WINDOWS], Y)
+                ms.append(win.timings())
+            win.set_profiling(False)
+            out[f"kernel_us_mean_{label}_tier"] = 1e3 * statistics.mean(ms)
+        B.check(B.strata_window_set_tier(win.handle, None), "strata_window_set_tier")
+        st, state = B.strata_tier_read(tier, E)
+        B.check(st, "strata_tier_read")
+        out.update(T=T, windows=steps, rounds=int(state["rounds"]), last_round_swaps=int(state["n_swaps"]),
+                   overhead_us=out["kernel_us_mean_with_tier"] - out["kernel_us_mean_without_tier"],
+                   tier="capacity E/2, a round every 4 windows, up to 8 swaps, decay 0.5, min gain 1.5")
+    finally:
+        B.strata_window_set_tier(win.handle, None)
+        B.strata_tier_destroy(tier)
+    return out
 
 
 def measure_workload(name, Ts, dev, flush, stream, peak, cpu_jobs=None, steps=300):

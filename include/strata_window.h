@@ -289,6 +289,70 @@ strata_status strata_stack_destroy(strata_stack* s);
 strata_status strata_moe_window_forward_noalloc(strata_window* h, const float* x, int32_t T, float* y,
                                                 void* cuda_stream);
 
+/* ---------------------------------------------------------------------------
+ * Routing counters of an adaptive expert tier.
+ *
+ * The Strata docs ("BATCHING.md", "Several requests at once (batch slots)",
+ * the adaptive expert tier paragraphs): batch windows count which experts
+ * they route to, and every --adapt-every windows (default 4) the engine swaps
+ * the most-routed experts that are not in the fast tier into it in place of
+ * the least-routed resident ones; --adapt-swaps bounds a round's swaps,
+ * --adapt-decay ages the counts, and --adapt-min-gain F (default 1.5) is the
+ * bar a swap must clear (incoming count against outgoing count).  A tier
+ * matters where the experts do not all fit the fast memory; this library keeps
+ * every expert in HBM and computes the same window either way, so a tier here
+ * is the bookkeeping a caller uses to place experts elsewhere.
+ *
+ * The readings this library implements (the pages leave them open):
+ *   c_e += entries routed to e by the window                      (fp32)
+ *   after the counts of every adapt_every-th window, a round: experts outside
+ *   the tier by c descending and tier experts by c ascending (ties to the
+ *   lower expert) pair up in order; pair i swaps while i < adapt_swaps and
+ *   c_in > c_out and c_in >= min_gain * c_out (fp32); the first pair that
+ *   fails ends the round; then every c_e *= decay                 (fp32)
+ * The window kernel's first CTA does this at the end of every window of a
+ * handle the tier is attached to (strata_window_set_tier), on the device.
+ * ------------------------------------------------------------------------- */
+typedef struct strata_tier strata_tier;
+
+typedef struct {
+  int32_t n_experts;    /* E of the layer it follows: 1..256 */
+  int32_t capacity;     /* experts the tier holds: 1..E */
+  int32_t adapt_every;  /* a round after every this many windows: >= 1 */
+  int32_t adapt_swaps;  /* most swaps per round: 0..E */
+  float decay;          /* every counter is multiplied by this after a round: (0, 1] */
+  float min_gain;       /* the swap bar: finite, >= 1 */
+} strata_tier_desc;
+
+typedef struct {
+  int64_t windows;      /* windows counted */
+  int64_t rounds;       /* rounds run */
+  int32_t n_swaps;      /* swaps made by the last round */
+} strata_tier_stats;
+
+/* Create a tier on the current device with zero counters.
+ *   initial: host array of `capacity` distinct experts the tier starts with,
+ *   or NULL for experts 0..capacity-1.
+ * Returns EINVAL (bad field or initial list), ENOMEM, ECUDA. */
+strata_status strata_tier_create(const strata_tier_desc* desc, const int32_t* initial, strata_tier** out);
+
+/* Attach a tier to a window handle (NULL detaches).  Every later window of
+ * the handle (plain, graph-cache and allocation-free entry points) updates it;
+ * the handle's cached graphs are dropped.  One tier per handle; the tier must
+ * outlive the attachment.  Returns EINVAL if n_experts differs from the
+ * handle's E. */
+strata_status strata_window_set_tier(strata_window* h, strata_tier* tier);
+
+/* Wait for the device, then copy the tier's state to host arrays (each may
+ * be NULL): counters float [E], resident int32 [E] (1 = in the tier),
+ * swap_in / swap_out int32 [E] (the last round's swaps, pairwise, first
+ * stats->n_swaps valid), stats. */
+strata_status strata_tier_read(strata_tier* tier, float* counters, int32_t* resident, int32_t* swap_in,
+                               int32_t* swap_out, strata_tier_stats* stats);
+
+/* Free a tier (detach it from its handle first).  NULL is accepted. */
+strata_status strata_tier_destroy(strata_tier* tier);
+
 /* Free the handle and everything it owns.  NULL is accepted (returns OK). */
 strata_status strata_window_destroy(strata_window* h);
 

@@ -24,7 +24,8 @@ EXPORTED = ("strata_window_create", "strata_moe_window_forward", "strata_window_
             "strata_window_set_profiling", "strata_window_timings", "strata_window_destroy", "strata_status_str",
             "strata_moe_window_forward_noalloc", "strata_moe_window_forward_graph", "strata_stack_create", "strata_stack_forward", "strata_stack_sync",
             "strata_stack_query", "strata_stack_set_profiling", "strata_stack_timings", "strata_stack_destroy",
-            "strata_window_plan")
+            "strata_window_plan", "strata_tier_create", "strata_window_set_tier", "strata_tier_read",
+            "strata_tier_destroy")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -77,6 +78,15 @@ class strata_stack_info(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("n_sm", ctypes.c_int32), ("stages", ctypes.c_int32),
                 ("stage_bytes", ctypes.c_int32), ("smem_bytes", ctypes.c_int32), ("dense_bytes", ctypes.c_int64),
                 ("expert_bytes", ctypes.c_int64), ("shared_bytes", ctypes.c_int64), ("router_bytes", ctypes.c_int64)]
+
+
+class strata_tier_desc(ctypes.Structure):
+    _fields_ = [("n_experts", ctypes.c_int32), ("capacity", ctypes.c_int32), ("adapt_every", ctypes.c_int32),
+                ("adapt_swaps", ctypes.c_int32), ("decay", ctypes.c_float), ("min_gain", ctypes.c_float)]
+
+
+class strata_tier_stats(ctypes.Structure):
+    _fields_ = [("windows", ctypes.c_int64), ("rounds", ctypes.c_int64), ("n_swaps", ctypes.c_int32)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -133,6 +143,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.strata_window_timings.restype = ctypes.c_int
     lib.strata_window_destroy.argtypes = [ctypes.c_void_p]
     lib.strata_window_destroy.restype = ctypes.c_int
+    lib.strata_tier_create.argtypes = [P(strata_tier_desc), ctypes.c_void_p, P(ctypes.c_void_p)]
+    lib.strata_tier_create.restype = ctypes.c_int
+    lib.strata_window_set_tier.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.strata_window_set_tier.restype = ctypes.c_int
+    lib.strata_tier_read.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_void_p, P(strata_tier_stats)]
+    lib.strata_tier_read.restype = ctypes.c_int
+    lib.strata_tier_destroy.argtypes = [ctypes.c_void_p]
+    lib.strata_tier_destroy.restype = ctypes.c_int
     lib.strata_status_str.argtypes = [ctypes.c_int]
     lib.strata_status_str.restype = ctypes.c_char_p
     _lib = lib
@@ -240,6 +259,38 @@ def strata_window_timings(handle):
 
 def strata_window_destroy(handle) -> int:
     return load().strata_window_destroy(ctypes.c_void_p(handle))
+
+
+def strata_tier_create(desc: strata_tier_desc, initial=None):
+    """initial: a sequence of expert ids or None.  Returns (status, tier or None)."""
+    h = ctypes.c_void_p()
+    arr = None
+    if initial is not None:
+        arr = (ctypes.c_int32 * len(initial))(*[int(e) for e in initial])
+    st = load().strata_tier_create(ctypes.byref(desc), arr, ctypes.byref(h))
+    return st, (h.value if st == STRATA_OK else None)
+
+
+def strata_window_set_tier(handle, tier) -> int:
+    return load().strata_window_set_tier(ctypes.c_void_p(handle), ctypes.c_void_p(tier) if tier else None)
+
+
+def strata_tier_read(tier, n_experts: int):
+    """Returns (status, dict of numpy arrays counters/resident/swap_in/swap_out and the stats)."""
+    import numpy as np
+    c = np.zeros(n_experts, np.float32)
+    r = np.zeros(n_experts, np.int32)
+    si = np.zeros(n_experts, np.int32)
+    so = np.zeros(n_experts, np.int32)
+    stats = strata_tier_stats()
+    st = load().strata_tier_read(ctypes.c_void_p(tier), c.ctypes.data, r.ctypes.data, si.ctypes.data, so.ctypes.data,
+                                 ctypes.byref(stats))
+    return st, dict(counters=c, resident=r, swap_in=si[:stats.n_swaps], swap_out=so[:stats.n_swaps],
+                    windows=stats.windows, rounds=stats.rounds, n_swaps=stats.n_swaps)
+
+
+def strata_tier_destroy(tier) -> int:
+    return load().strata_tier_destroy(ctypes.c_void_p(tier) if tier else None)
 
 
 def check(status: int, what: str) -> None:

@@ -88,6 +88,22 @@ struct LayerDev {
   int kph_log2, kpg_log2;  // log2 of the o-projection k-steps per head / per kv group
 };
 
+// Adaptive expert tier state that windows update (device pointers; a null
+// `counters` means no tier is attached).  Counters are fp32 routed-entry
+// counts aged by `decay` after every round; a round every `adapt_every`
+// windows swaps up to `adapt_swaps` experts between the tier and the rest.
+struct TierDev {
+  float* counters;          // [E]
+  int* resident;            // [E] 1 = in the tier
+  long long* windows;       // windows counted so far
+  long long* rounds;        // rounds run so far
+  int* n_swaps;             // swaps made by the last round
+  int* swap_in;             // [E] experts the last round moved in (first n_swaps)
+  int* swap_out;            // [E] experts it moved out, pairwise with swap_in
+  int adapt_every, adapt_swaps;
+  float decay, min_gain;
+};
+
 struct WindowBufs {
   const float* x;          // [T][d]
   float* y;                // [T][d]
@@ -113,6 +129,7 @@ struct WindowBufs {
   float* partial;          // router partial logits [njb][kMaxRows][E]
   int njb;                 // column chunks of the router GEMV
   unsigned* err;
+  TierDev tier;            // adaptive tier bookkeeping (single-layer windows; counters null = none)
   long long wait_cycles;   // limit of every bounded device wait, in SM clock cycles
   int bar_extra;           // arrivals a grid barrier expects beyond the grid (0; > 0 only in failure tests)
   // decoder-layer extras (stack kernel only; null in the single-layer kernel)

@@ -1650,6 +1650,75 @@ __device__ __noinline__ void combine_all(const LayerDev& L, const WindowBufs& W)
   }
 }
 
+// The adaptive tier's bookkeeping for one window, by all threads of CTA 0
+// once the window's work is done.  The Strata docs ("BATCHING.md", the
+// adaptive expert tier paragraphs) have batch windows count the experts they
+// route to and, every --adapt-every windows, swap the most-routed experts
+// outside the fast tier with the least-routed ones inside, up to
+// --adapt-swaps, a swap needing the incoming count to clear --adapt-min-gain
+// times the outgoing one, with --adapt-decay aging the counts.  Here:
+//   c_e += (entries routed to e in this window)            (fp32)
+//   every adapt_every-th window: outside experts by c descending and tier
+//   experts by c ascending (ties to the lower expert) pair up in order; pair i
+//   swaps while i < adapt_swaps, c_in > c_out and c_in >= min_gain * c_out
+//   (the first pair that fails ends the round); then c_e *= decay.
+// scratch: 4 x kMaxExperts words of shared memory that nothing else uses now.
+__device__ __noinline__ void tier_step(const TierDev& Tr, const SPlan& sp, int E, uint8_t* scratch) {
+  float* c = reinterpret_cast<float*>(scratch);
+  int* res = reinterpret_cast<int*>(c + kMaxExperts);
+  int* by_in = res + kMaxExperts;
+  int* by_out = by_in + kMaxExperts;
+  __shared__ int s_round;
+  const int tid = threadIdx.x;
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    const float v = __fadd_rn(Tr.counters[e], (float)sp.counts[e]);
+    Tr.counters[e] = v;
+    c[e] = v;
+    res[e] = Tr.resident[e];
+  }
+  if (tid == 0) {
+    const long long w = *Tr.windows + 1;
+    *Tr.windows = w;
+    s_round = (Tr.adapt_every > 0 && w % Tr.adapt_every == 0) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_round) return;
+  for (int e = tid; e < E; e += blockDim.x) {
+    const float ce = c[e];
+    const int re = res[e];
+    int rank = 0;
+    for (int f = 0; f < E; ++f) {
+      if (res[f] != re) continue;
+      const float cf = c[f];
+      rank += re ? (cf < ce || (cf == ce && f < e)) : (cf > ce || (cf == ce && f < e));
+    }
+    (re ? by_out : by_in)[rank] = e;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int n_out = 0;
+    for (int e = 0; e < E; ++e) n_out += res[e] ? 1 : 0;
+    const int n_in = E - n_out;
+    const int lim = min(Tr.adapt_swaps, min(n_in, n_out));
+    int n = 0;
+    while (n < lim) {
+      const float ca = c[by_in[n]], cb = c[by_out[n]];
+      if (ca > cb && ca >= __fmul_rn(Tr.min_gain, cb)) ++n;
+      else break;
+    }
+    for (int i = 0; i < n; ++i) {
+      Tr.resident[by_in[i]] = 1;
+      Tr.resident[by_out[i]] = 0;
+      Tr.swap_in[i] = by_in[i];
+      Tr.swap_out[i] = by_out[i];
+    }
+    *Tr.n_swaps = n;
+    *Tr.rounds += 1;
+  }
+  for (int e = tid; e < E; e += blockDim.x) Tr.counters[e] = __fmul_rn(c[e], Tr.decay);
+}
+
 // The producer thread's drain after an abort: every copy it issued lands
 // before the CTA may move on or exit.
 __device__ __noinline__ void drain_ring(const Ring& rg, const KernelCfg& C, const RingPos& rp, long long limit) {
@@ -1865,6 +1934,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) window_kernel(LayerDev L, W
     combine_all(L, W);
     STAMP(0, 16);
   }
+  if (blockIdx.x == 0 && W.tier.counters) tier_step(W.tier, sp, L.E, m.ring);
 }
 
 // The window kernel on the register-fed path: 16 warps, no producer warp and
@@ -1887,6 +1957,7 @@ __global__ void __launch_bounds__(kConsumerThreads, 1) window_kernel_direct(Laye
     if (!grid_barrier(W, &sp.ok) || s_abort) return;
     combine_all(L, W);
   }
+  if (blockIdx.x == 0 && W.tier.counters) tier_step(W.tier, sp, L.E, m.ring);
 }
 
 // A window through n decoder layers in one launch.  Per layer:

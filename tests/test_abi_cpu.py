@@ -189,3 +189,26 @@ def test_plan_keeps_the_ring_when_a_warp_would_get_no_k_step(lib, monkeypatch, f
     assert st == B.STRATA_OK and forced.stages >= 2
     wide = wlm.MoESpec(4096, 16, 2, 1024, 512, 4, 32)
     assert _plan(wide, monkeypatch)[1].stages == 1
+
+
+@pytest.mark.parametrize("kw", [
+    dict(n_experts=0), dict(n_experts=300), dict(capacity=0), dict(capacity=17), dict(adapt_every=0),
+    dict(adapt_swaps=-1), dict(adapt_swaps=17), dict(decay=0.0), dict(decay=1.5), dict(min_gain=0.5),
+    dict(min_gain=float("inf")), dict(min_gain=float("nan")),
+])
+def test_tier_create_rejects_bad_desc_on_host(lib, kw):
+    base = dict(n_experts=16, capacity=4, adapt_every=4, adapt_swaps=2, decay=0.5, min_gain=1.5)
+    base.update(kw)
+    st, t = B.strata_tier_create(B.strata_tier_desc(**base))
+    assert st == B.STRATA_EINVAL and t is None
+
+
+@pytest.mark.parametrize("initial", [[0, 1, 1, 2], [0, 1, 2, 16], [-1, 0, 1, 2]])
+def test_tier_create_rejects_a_bad_initial_list_on_host(lib, initial):
+    st, t = B.strata_tier_create(B.strata_tier_desc(16, 4, 4, 2, 0.5, 1.5), initial)
+    assert st == B.STRATA_EINVAL and t is None
+
+
+def test_tier_calls_accept_null(lib):
+    assert B.strata_tier_destroy(None) == B.STRATA_OK
+    assert B.strata_window_set_tier(None, None) == B.STRATA_EINVAL
