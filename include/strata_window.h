@@ -290,6 +290,82 @@ strata_status strata_moe_window_forward_noalloc(strata_window* h, const float* x
                                                 void* cuda_stream);
 
 /* ---------------------------------------------------------------------------
+ * The window's output head, each row's token and each slot's proposal check.
+ *
+ * The Strata docs ("BATCHING.md", "Several requests at once (batch slots)"):
+ * the head is among the weights a verify window reads once for all of its
+ * rows (opening paragraph); sampled requests draw every row with the solo
+ * window's counter-based draw, Philox(seed, position) (section "Exactness");
+ * with --batch-mtp a window carries two rows per slot, its token and its MTP
+ * proposal, and checks the proposal (--batch-mtp paragraph).  The readings
+ * this library implements (the pages give no formulas):
+ *   logits[t] = W_head RMSNorm(x_t), RMSNorm(x) = x / sqrt(mean(x^2) + 1e-6)
+ *   temperature <= 0: token = argmax (ties to the lower token)
+ *   temperature > 0: u = (Philox4x64-10(counter (position, 0, 0, 0),
+ *     key (seed, 0)) word 0 >> 40) * 2^-24; token = the first v whose
+ *     cumulative softmax(logits / temperature) weight exceeds u times the
+ *     total (fp32, the vocabulary summed in fixed slices); the greedy token
+ *     should rounding leave no token above it
+ *   a slot's rows are consecutive; its first row has fed = -1, each later row
+ *   was fed a proposal; the slot emits its first row's token and then, while
+ *   the previous row's token equals the proposal a row was fed, that row's
+ *   token too (n_emit at the slot's first row; 0 at its other rows).
+ * ------------------------------------------------------------------------- */
+typedef struct strata_head strata_head;
+
+typedef struct {
+  int32_t hidden;    /* d: multiple of 64 (4-bit) or 128 (2-bit) */
+  int32_t vocab;     /* V: multiple of 16, at most 2^22 */
+  int32_t bits;      /* 4 (block 32) or 2 (block 16) */
+  int32_t block;
+  int32_t max_rows;  /* 1..8 */
+} strata_head_desc;
+
+/* Per-row draw inputs (device arrays of the window's T rows). */
+typedef struct {
+  const int32_t* position;     /* the position whose token the row draws (Philox counter) */
+  const uint64_t* seed;        /* the row's seed (Philox key) */
+  const float* temperature;    /* <= 0: greedy */
+  const int32_t* fed;          /* the proposal the row was fed, -1 for a slot's first row */
+} strata_draw_in;
+
+/* Per-row outputs (device arrays). */
+typedef struct {
+  int32_t* tokens;   /* [T] each row's token */
+  int32_t* n_emit;   /* [T] tokens each slot emits, at its first row; 0 at its other rows */
+  float* logits;     /* [T][V] the logits, or NULL (then they stay in the handle's workspace) */
+} strata_draw_out;
+
+/* Create a head on the current device.  weight: device block-format matrix
+ * [1][V][d] (copied into the handle's kernel-ordered layout; the caller may
+ * free it once create returns), read on cuda_stream.  Returns EINVAL,
+ * EUNSUPPORTED, ENOMEM, ECUDA. */
+strata_status strata_head_create(const strata_head_desc* desc, const strata_qmat* weight, void* cuda_stream,
+                                 strata_head** out);
+
+/* One window's head: x device fp32 [T][d] (16-byte aligned), 1 <= T <=
+ * max_rows; in and out as above.  Asynchronous on cuda_stream; one
+ * cooperative launch.  Device errors (a non-finite logit, a wait that gave up)
+ * are reported by strata_head_sync.  Returns EINVAL before any launch for bad
+ * arguments, ECUDA if the launch fails. */
+strata_status strata_head_forward(strata_head* h, const float* x, int32_t T, const strata_draw_in* in,
+                                  const strata_draw_out* out, void* cuda_stream);
+
+/* Wait for the last head_forward; EDEVICE (once) if the GPU recorded an error. */
+strata_status strata_head_sync(strata_head* h);
+
+/* Block-format bytes of the head matrix and the handle's workspace bytes
+ * (either pointer may be NULL). */
+strata_status strata_head_query(const strata_head* h, int64_t* head_bytes, int64_t* workspace_bytes);
+
+/* Measurement aid, as strata_window_set_profiling / strata_window_timings. */
+strata_status strata_head_set_profiling(strata_head* h, int32_t enable);
+strata_status strata_head_timings(strata_head* h, float* ms);
+
+/* Free a head.  NULL is accepted. */
+strata_status strata_head_destroy(strata_head* h);
+
+/* ---------------------------------------------------------------------------
  * Routing counters of an adaptive expert tier.
  *
  * The Strata docs ("BATCHING.md", "Several requests at once (batch slots)",
@@ -310,8 +386,12 @@ strata_status strata_moe_window_forward_noalloc(strata_window* h, const float* x
  *   lower expert) pair up in order; pair i swaps while i < adapt_swaps and
  *   c_in > c_out and c_in >= min_gain * c_out (fp32); the first pair that
  *   fails ends the round; then every c_e *= decay                 (fp32)
- * The window kernel's first CTA does this at the end of every window of a
- * handle the tier is attached to (strata_window_set_tier), on the device.
+ * All of it runs on the device, in the window kernel of a handle the tier is
+ * attached to (strata_window_set_tier): its first CTA adds the window's
+ * counts while it forms the routing plan, and runs a round that is due while
+ * it waits at the next window's first grid barrier, before that window's
+ * counts; strata_tier_read runs a due round itself before it copies, so what
+ * it reports is always the state after the rounds of the windows so far.
  * ------------------------------------------------------------------------- */
 typedef struct strata_tier strata_tier;
 
@@ -341,12 +421,16 @@ strata_status strata_tier_create(const strata_tier_desc* desc, const int32_t* in
  * the handle's cached graphs are dropped.  One tier per handle; the tier must
  * outlive the attachment.  Returns EINVAL if n_experts differs from the
  * handle's E. */
+/* (EUNSUPPORTED if the handle's shared-memory ring is too small to hold a
+ * round's arrays beside the staged rows of x; no layer shape here comes near.) */
 strata_status strata_window_set_tier(strata_window* h, strata_tier* tier);
 
-/* Wait for the device, then copy the tier's state to host arrays (each may
- * be NULL): counters float [E], resident int32 [E] (1 = in the tier),
- * swap_in / swap_out int32 [E] (the last round's swaps, pairwise, first
- * stats->n_swaps valid), stats. */
+/* Wait for the device, run the round that is due (if the last window
+ * completed a multiple of adapt_every windows and its round has not run yet),
+ * then copy the tier's state to host arrays (each may be NULL): counters
+ * float [E], resident int32 [E] (1 = in the tier), swap_in / swap_out int32
+ * [E] (the last round's swaps, pairwise, first stats->n_swaps valid), stats.
+ * No window of the attached handle may run meanwhile. */
 strata_status strata_tier_read(strata_tier* tier, float* counters, int32_t* resident, int32_t* swap_in,
                                int32_t* swap_out, strata_tier_stats* stats);
 

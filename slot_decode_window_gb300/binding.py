@@ -25,7 +25,8 @@ EXPORTED = ("strata_window_create", "strata_moe_window_forward", "strata_window_
             "strata_moe_window_forward_noalloc", "strata_moe_window_forward_graph", "strata_stack_create", "strata_stack_forward", "strata_stack_sync",
             "strata_stack_query", "strata_stack_set_profiling", "strata_stack_timings", "strata_stack_destroy",
             "strata_window_plan", "strata_tier_create", "strata_window_set_tier", "strata_tier_read",
-            "strata_tier_destroy")
+            "strata_tier_destroy", "strata_head_create", "strata_head_forward", "strata_head_sync",
+            "strata_head_query", "strata_head_set_profiling", "strata_head_timings", "strata_head_destroy")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -87,6 +88,18 @@ class strata_tier_desc(ctypes.Structure):
 
 class strata_tier_stats(ctypes.Structure):
     _fields_ = [("windows", ctypes.c_int64), ("rounds", ctypes.c_int64), ("n_swaps", ctypes.c_int32)]
+
+
+class strata_head_desc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("hidden", "vocab", "bits", "block", "max_rows")]
+
+
+class strata_draw_in(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("position", "seed", "temperature", "fed")]
+
+
+class strata_draw_out(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("tokens", "n_emit", "logits")]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -152,6 +165,21 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.strata_tier_read.restype = ctypes.c_int
     lib.strata_tier_destroy.argtypes = [ctypes.c_void_p]
     lib.strata_tier_destroy.restype = ctypes.c_int
+    lib.strata_head_create.argtypes = [P(strata_head_desc), P(strata_qmat), ctypes.c_void_p, P(ctypes.c_void_p)]
+    lib.strata_head_create.restype = ctypes.c_int
+    lib.strata_head_forward.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, P(strata_draw_in),
+                                        P(strata_draw_out), ctypes.c_void_p]
+    lib.strata_head_forward.restype = ctypes.c_int
+    lib.strata_head_sync.argtypes = [ctypes.c_void_p]
+    lib.strata_head_sync.restype = ctypes.c_int
+    lib.strata_head_query.argtypes = [ctypes.c_void_p, P(ctypes.c_int64), P(ctypes.c_int64)]
+    lib.strata_head_query.restype = ctypes.c_int
+    lib.strata_head_set_profiling.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+    lib.strata_head_set_profiling.restype = ctypes.c_int
+    lib.strata_head_timings.argtypes = [ctypes.c_void_p, P(ctypes.c_float)]
+    lib.strata_head_timings.restype = ctypes.c_int
+    lib.strata_head_destroy.argtypes = [ctypes.c_void_p]
+    lib.strata_head_destroy.restype = ctypes.c_int
     lib.strata_status_str.argtypes = [ctypes.c_int]
     lib.strata_status_str.restype = ctypes.c_char_p
     _lib = lib
@@ -291,6 +319,43 @@ def strata_tier_read(tier, n_experts: int):
 
 def strata_tier_destroy(tier) -> int:
     return load().strata_tier_destroy(ctypes.c_void_p(tier) if tier else None)
+
+
+def strata_head_create(desc: strata_head_desc, weight: strata_qmat, stream: int = 0):
+    """Returns (status, head or None)."""
+    h = ctypes.c_void_p()
+    st = load().strata_head_create(ctypes.byref(desc), ctypes.byref(weight), ctypes.c_void_p(stream), ctypes.byref(h))
+    return st, (h.value if st == STRATA_OK else None)
+
+
+def strata_head_forward(handle, x_ptr: int, T: int, draw_in: strata_draw_in, draw_out: strata_draw_out,
+                        stream: int = 0) -> int:
+    return load().strata_head_forward(ctypes.c_void_p(handle), ctypes.c_void_p(x_ptr), T, ctypes.byref(draw_in),
+                                      ctypes.byref(draw_out), ctypes.c_void_p(stream))
+
+
+def strata_head_sync(handle) -> int:
+    return load().strata_head_sync(ctypes.c_void_p(handle))
+
+
+def strata_head_query(handle):
+    hb, wb = ctypes.c_int64(), ctypes.c_int64()
+    st = load().strata_head_query(ctypes.c_void_p(handle), ctypes.byref(hb), ctypes.byref(wb))
+    return st, hb.value, wb.value
+
+
+def strata_head_set_profiling(handle, enable: bool) -> int:
+    return load().strata_head_set_profiling(ctypes.c_void_p(handle), 1 if enable else 0)
+
+
+def strata_head_timings(handle):
+    ms = ctypes.c_float()
+    st = load().strata_head_timings(ctypes.c_void_p(handle), ctypes.byref(ms))
+    return st, ms.value
+
+
+def strata_head_destroy(handle) -> int:
+    return load().strata_head_destroy(ctypes.c_void_p(handle) if handle else None)
 
 
 def check(status: int, what: str) -> None:
@@ -465,6 +530,63 @@ class Stack:
     def close(self) -> None:
         if getattr(self, "handle", None):
             strata_stack_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Head:
+    """The output head for a block-format weight ``QMat`` [1][V][d] on the GPU."""
+
+    def __init__(self, weight, max_rows: int = 8, stream=None):
+        import torch
+        self.V, self.d = weight.rows, weight.cols
+        s = (stream or torch.cuda.current_stream()).cuda_stream
+        desc = strata_head_desc(weight.cols, weight.rows, weight.bits, weight.block, max_rows)
+        st, h = strata_head_create(desc, _qmat(weight), s)
+        check(st, "strata_head_create")
+        self.handle = h
+
+    def forward(self, x, position, seed, temperature, fed, logits: bool = False, stream=None):
+        """Enqueue one window's head on x [T][d]; the per-row inputs are CUDA
+        tensors (int32, int64 seeds, float32, int32).  Returns (tokens, n_emit,
+        logits or None), int32 / float32 CUDA tensors."""
+        import torch
+        assert x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()
+        T = x.shape[0]
+        dev = x.device
+        tokens = torch.empty(T, dtype=torch.int32, device=dev)
+        n_emit = torch.empty(T, dtype=torch.int32, device=dev)
+        lg = torch.empty(T, self.V, device=dev) if logits else None
+        di = strata_draw_in(position.data_ptr(), seed.data_ptr(), temperature.data_ptr(), fed.data_ptr())
+        do = strata_draw_out(tokens.data_ptr(), n_emit.data_ptr(), lg.data_ptr() if logits else None)
+        s = (stream or torch.cuda.current_stream()).cuda_stream
+        check(strata_head_forward(self.handle, x.data_ptr(), T, di, do, s), "strata_head_forward")
+        return tokens, n_emit, lg
+
+    def sync(self) -> None:
+        check(strata_head_sync(self.handle), "strata_head_sync")
+
+    def set_profiling(self, enable: bool) -> None:
+        check(strata_head_set_profiling(self.handle, enable), "strata_head_set_profiling")
+
+    def timings(self):
+        st, ms = strata_head_timings(self.handle)
+        check(st, "strata_head_timings")
+        return ms
+
+    def head_bytes(self) -> int:
+        st, hb, _ = strata_head_query(self.handle)
+        check(st, "strata_head_query")
+        return hb
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            strata_head_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

@@ -141,6 +141,21 @@ struct WindowBufs {
   float* k_out;            // [T][dkv] or null
 };
 
+// Per-row token draw of the output head and its proposal check (head kernel
+// only; all device pointers, arrays of the window's T rows).
+struct HeadArgs {
+  const int* position;               // [T] position whose token the row draws (Philox counter)
+  const unsigned long long* seed;    // [T] the row's seed (Philox key)
+  const float* temperature;          // [T] <= 0: greedy
+  const int* fed;                    // [T] the proposal the row was fed; -1 for a slot's first row
+  int* tokens;                       // [T] out: the row's token
+  int* n_emit;                       // [T] out: tokens the slot emits, at its first row (0 elsewhere)
+  float* part_max;                   // [grid][kMaxRows] scratch: per-CTA slice maxima
+  int* part_arg;                     // [grid][kMaxRows] scratch: their tokens
+  float* part_sum;                   // [grid][kMaxRows] scratch: per-CTA slice sums of exp
+  int V;                             // vocabulary (rows of the head matrix)
+};
+
 constexpr int kMaxChunks = 32;  // k-chunks per tile
 
 // How one phase (0 gate/up, 1 down, 2 dense q/k/v, 3 dense o) cuts its tiles

@@ -25,6 +25,18 @@ cudaError_t launch_stack(const LayerDev* layers, int n_layers, int bits, const W
                          int grid, const float* x, float* y, float* ybuf, float* q_all, float* k_all,
                          cudaStream_t s);
 
+// The output head of a window: RMSNorm, the head GEMV over V rows (L.qkv the
+// packed head matrix, L.dq = V, W.q_out the logits [T][V]), each row's token
+// and each slot's proposal check, in one cooperative launch.
+KernelCfg head_cfg(int d, int bits, int max_rows, int smem_limit);
+cudaError_t head_set_attrs(int bits, int smem_bytes);
+int head_blocks_per_sm(int bits, int smem_bytes);
+cudaError_t launch_head(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, const HeadArgs& H, int grid,
+                        cudaStream_t s);
+
+// The adaptive tier's round that is due, if any, in a one-CTA launch.
+cudaError_t launch_tier_round(const TierDev& Tr, int E, cudaStream_t s);
+
 // Repack one canonical block-quantized matrix stack into the tile format.
 cudaError_t launch_repack(const uint8_t* codes, const uint16_t* scale, const uint16_t* mn, int n, int rows, int K,
                           int bits, uint8_t* out, cudaStream_t s);

@@ -1,13 +1,15 @@
 // C ABI of the adaptive expert tier's bookkeeping: a tier object holds fp32
 // routing counters, the set of experts in the fast tier and the last round's
-// swaps on the device; a window handle it is attached to updates it at the
-// end of every window (tier_step in window.cu).
+// swaps on the device; the window kernel of a handle it is attached to adds
+// each window's counts and runs the rounds (tier_count, tier_round_due in
+// window.cu).
 #include <cstring>
 #include <new>
 #include <vector>
 
 #include "common.cuh"
 #include "handle.h"
+#include "kernels.h"
 #include "strata_window.h"
 
 using namespace strata;
@@ -91,6 +93,10 @@ strata_status strata_tier_create(const strata_tier_desc* desc, const int32_t* in
 strata_status strata_window_set_tier(strata_window* h, strata_tier* t) {
   if (!h) return STRATA_EINVAL;
   if (t && t->desc.n_experts != h->desc.n_experts) return STRATA_EINVAL;
+  // a due round keeps four expert arrays in the ring region beside stage R's
+  // staged rows of x (8 rows x 512 floats)
+  if (t && (long long)h->cfg.nstages * h->cfg.stage_bytes < 8 * 512 * 4 + 4 * kMaxExperts * 4)
+    return STRATA_EUNSUPPORTED;
   // cached graphs hold the window's arguments by value: drop them
   for (strata_graph_entry& g : h->graphs) {
     if (g.exec) cudaGraphExecDestroy(g.exec);
@@ -104,7 +110,11 @@ strata_status strata_tier_read(strata_tier* t, float* counters, int32_t* residen
                                int32_t* swap_out, strata_tier_stats* stats) {
   if (!t) return STRATA_EINVAL;
   const size_t E = (size_t)t->desc.n_experts;
+  // a round that is due after the last window has not run yet (the next
+  // window would run it before adding its own counts): run it now
   cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = launch_tier_round(t->dev, (int)E, nullptr);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e == cudaSuccess && counters) e = cudaMemcpy(counters, t->dev.counters, E * 4, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess && resident) e = cudaMemcpy(resident, t->dev.resident, E * 4, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess && swap_in) e = cudaMemcpy(swap_in, t->dev.swap_in, E * 4, cudaMemcpyDeviceToHost);

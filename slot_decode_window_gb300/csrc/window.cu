@@ -48,6 +48,9 @@ namespace strata {
 namespace {
 
 constexpr int kMaxSub = 4;  // sub-tiles per task
+// Where a due tier round keeps its arrays in the ring region while stage R's
+// staged rows of x (kMaxRows x kRouterCols floats) still sit at its start.
+constexpr int kTierScratchOff = kMaxRows * kRouterCols * 4;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 
 // Stage timestamps for timing builds (-DSTRATA_STAMPS): one lane of the CTA
@@ -516,13 +519,22 @@ __device__ __noinline__ void router_stage(const LayerDev& L, const WindowBufs& W
 // All CTAs arrive; thread 0 waits (bounded) until every CTA of this window has.
 // The counter only grows: the window's target is the next multiple of the grid
 // (plus W.bar_extra, which is 0 except in tests that make the wait run out).
-__device__ bool grid_barrier(const WindowBufs& W, int* s_ok) {
+// grid_barrier_split arrives, runs `between` with all threads of the CTA, and
+// then waits.
+template <typename F>
+__device__ bool grid_barrier_split(const WindowBufs& W, int* s_ok, F between) {
+  __shared__ unsigned long long s_target;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     const unsigned long long n = gridDim.x;
     const unsigned long long old = atomicAdd(W.gbar, 1ull);
-    const unsigned long long target = (old / n + 1) * n + (unsigned long long)W.bar_extra;
+    s_target = (old / n + 1) * n + (unsigned long long)W.bar_extra;
+  }
+  between();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned long long target = s_target;
     const long long t0 = clock64();
     int ok = 1;
     while (ld_acquire_u64(W.gbar) < target) {
@@ -538,6 +550,10 @@ __device__ bool grid_barrier(const WindowBufs& W, int* s_ok) {
   }
   __syncthreads();
   return *s_ok != 0;
+}
+
+__device__ __forceinline__ bool grid_barrier(const WindowBufs& W, int* s_ok) {
+  return grid_barrier_split(W, s_ok, [] {});
 }
 
 // Row t (warp t; lane holds experts lane + 32 i): logits as the column-chunk
@@ -626,6 +642,98 @@ __device__ __forceinline__ void plan_row(const LayerDev& L, const WindowBufs& W,
   }
 }
 
+// The adaptive tier's bookkeeping.  The Strata docs ("BATCHING.md", the
+// adaptive expert tier paragraphs) have batch windows count the experts they
+// route to and, every --adapt-every windows, swap the most-routed experts
+// outside the fast tier with the least-routed ones inside, up to
+// --adapt-swaps, a swap needing the incoming count to clear --adapt-min-gain
+// times the outgoing one, with --adapt-decay aging the counts.  Here:
+//   c_e += (entries routed to e in this window)            (fp32)
+//   after every adapt_every-th window, a round: outside experts by c
+//   descending and tier experts by c ascending (ties to the lower expert)
+//   pair up in order; pair i swaps while i < adapt_swaps, c_in > c_out and
+//   c_in >= min_gain * c_out (the first pair that fails ends the round); then
+//   c_e *= decay.
+// The counts are added by CTA 0 during the plan with fire-and-forget atomics
+// (one adder per counter per window, so the fp32 sums are deterministic).  A
+// round that is due runs in CTA 0 of the next window while that CTA waits at
+// its first grid barrier (before the window's own counts are added), or in
+// strata_tier_read's one-CTA launch, whichever comes first: the rounds
+// counter says whether it has run.
+
+// CTA 0, during the plan: add the window's counts (threads e < E).
+__device__ __forceinline__ void tier_count(const TierDev& Tr, const SPlan& sp, int E) {
+  const int tid = threadIdx.x;
+  if (tid < E && sp.counts[tid] > 0) atomicAdd(Tr.counters + tid, (float)sp.counts[tid]);
+  if (tid == 0) atomicAdd(reinterpret_cast<unsigned long long*>(Tr.windows), 1ull);
+}
+
+// All threads of one CTA: run the round that is due, if any.  scratch: four
+// kMaxExperts-word arrays of shared memory nothing else uses meanwhile.
+__device__ __noinline__ void tier_round_due(const TierDev& Tr, int E, uint8_t* scratch) {
+  float* c = reinterpret_cast<float*>(scratch);
+  int* res = reinterpret_cast<int*>(c + kMaxExperts);
+  int* by_in = res + kMaxExperts;
+  int* by_out = by_in + kMaxExperts;
+  __shared__ int s_due;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    const long long w = *reinterpret_cast<volatile long long*>(Tr.windows);
+    const long long r = *reinterpret_cast<volatile long long*>(Tr.rounds);
+    s_due = (Tr.adapt_every > 0 && w / Tr.adapt_every > r) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_due) return;
+  for (int e = tid; e < E; e += blockDim.x) {
+    c[e] = __ldcg(Tr.counters + e);
+    res[e] = __ldcg(Tr.resident + e);
+  }
+  __syncthreads();
+  // ranks: four threads per expert, each counting a quarter of the others
+  const int per = blockDim.x >> 2, q = tid & 3;
+  const int iters = (E + per - 1) / per;
+  for (int it = 0; it < iters; ++it) {
+    const int e = it * per + (tid >> 2);
+    const bool valid = (tid >> 2) < per && e < E;
+    int rank = 0;
+    if (valid) {
+      const float ce = c[e];
+      const int re = res[e];
+      const int f0 = q * E / 4, f1 = (q + 1) * E / 4;
+      for (int f = f0; f < f1; ++f) {
+        if (res[f] != re) continue;
+        const float cf = c[f];
+        rank += re ? (cf < ce || (cf == ce && f < e)) : (cf > ce || (cf == ce && f < e));
+      }
+    }
+    rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+    rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+    if (valid && q == 0) (res[e] ? by_out : by_in)[rank] = e;
+  }
+  const int n_out = __syncthreads_count(tid < E && res[tid]);
+  if (tid == 0) {
+    const int n_in = E - n_out;
+    const int lim = min(Tr.adapt_swaps, min(n_in, n_out));
+    int n = 0;
+    while (n < lim) {
+      const float ca = c[by_in[n]], cb = c[by_out[n]];
+      if (ca > cb && ca >= __fmul_rn(Tr.min_gain, cb)) ++n;
+      else break;
+    }
+    for (int i = 0; i < n; ++i) {
+      Tr.resident[by_in[i]] = 1;
+      Tr.resident[by_out[i]] = 0;
+      Tr.swap_in[i] = by_in[i];
+      Tr.swap_out[i] = by_out[i];
+    }
+    *Tr.n_swaps = n;
+    *Tr.rounds += 1;
+  }
+  for (int e = tid; e < E; e += blockDim.x) Tr.counters[e] = __fmul_rn(c[e], Tr.decay);
+  __threadfence();
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
 // stage P: the routing plan (every CTA, same fixed-order arithmetic)
 // ---------------------------------------------------------------------------
@@ -691,6 +799,7 @@ __device__ __noinline__ void compute_plan(const LayerDev& L, const WindowBufs& W
     sp.entries[pos] = n_me;
     if (pub && W.out_entries) W.out_entries[pos] = n_me;
   }
+  if (pub && W.tier.counters) tier_count(W.tier, sp, E);
 }
 
 struct Task {
@@ -1650,75 +1759,6 @@ __device__ __noinline__ void combine_all(const LayerDev& L, const WindowBufs& W)
   }
 }
 
-// The adaptive tier's bookkeeping for one window, by all threads of CTA 0
-// once the window's work is done.  The Strata docs ("BATCHING.md", the
-// adaptive expert tier paragraphs) have batch windows count the experts they
-// route to and, every --adapt-every windows, swap the most-routed experts
-// outside the fast tier with the least-routed ones inside, up to
-// --adapt-swaps, a swap needing the incoming count to clear --adapt-min-gain
-// times the outgoing one, with --adapt-decay aging the counts.  Here:
-//   c_e += (entries routed to e in this window)            (fp32)
-//   every adapt_every-th window: outside experts by c descending and tier
-//   experts by c ascending (ties to the lower expert) pair up in order; pair i
-//   swaps while i < adapt_swaps, c_in > c_out and c_in >= min_gain * c_out
-//   (the first pair that fails ends the round); then c_e *= decay.
-// scratch: 4 x kMaxExperts words of shared memory that nothing else uses now.
-__device__ __noinline__ void tier_step(const TierDev& Tr, const SPlan& sp, int E, uint8_t* scratch) {
-  float* c = reinterpret_cast<float*>(scratch);
-  int* res = reinterpret_cast<int*>(c + kMaxExperts);
-  int* by_in = res + kMaxExperts;
-  int* by_out = by_in + kMaxExperts;
-  __shared__ int s_round;
-  const int tid = threadIdx.x;
-  __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
-    const float v = __fadd_rn(Tr.counters[e], (float)sp.counts[e]);
-    Tr.counters[e] = v;
-    c[e] = v;
-    res[e] = Tr.resident[e];
-  }
-  if (tid == 0) {
-    const long long w = *Tr.windows + 1;
-    *Tr.windows = w;
-    s_round = (Tr.adapt_every > 0 && w % Tr.adapt_every == 0) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!s_round) return;
-  for (int e = tid; e < E; e += blockDim.x) {
-    const float ce = c[e];
-    const int re = res[e];
-    int rank = 0;
-    for (int f = 0; f < E; ++f) {
-      if (res[f] != re) continue;
-      const float cf = c[f];
-      rank += re ? (cf < ce || (cf == ce && f < e)) : (cf > ce || (cf == ce && f < e));
-    }
-    (re ? by_out : by_in)[rank] = e;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int n_out = 0;
-    for (int e = 0; e < E; ++e) n_out += res[e] ? 1 : 0;
-    const int n_in = E - n_out;
-    const int lim = min(Tr.adapt_swaps, min(n_in, n_out));
-    int n = 0;
-    while (n < lim) {
-      const float ca = c[by_in[n]], cb = c[by_out[n]];
-      if (ca > cb && ca >= __fmul_rn(Tr.min_gain, cb)) ++n;
-      else break;
-    }
-    for (int i = 0; i < n; ++i) {
-      Tr.resident[by_in[i]] = 1;
-      Tr.resident[by_out[i]] = 0;
-      Tr.swap_in[i] = by_in[i];
-      Tr.swap_out[i] = by_out[i];
-    }
-    *Tr.n_swaps = n;
-    *Tr.rounds += 1;
-  }
-  for (int e = tid; e < E; e += blockDim.x) Tr.counters[e] = __fmul_rn(c[e], Tr.decay);
-}
-
 // The producer thread's drain after an abort: every copy it issued lands
 // before the CTA may move on or exit.
 __device__ __noinline__ void drain_ring(const Ring& rg, const KernelCfg& C, const RingPos& rp, long long limit) {
@@ -1923,7 +1963,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) window_kernel(LayerDev L, W
   __syncthreads();
   STAMP(0, 19);
 #endif
-  if (!grid_barrier(W, &sp.ok)) return;  // timed out: the error word says so
+  if (!grid_barrier_split(W, &sp.ok, [&] {
+        if (blockIdx.x == 0 && W.tier.counters) tier_round_due(W.tier, L.E, m.ring + kTierScratchOff);
+      }))
+    return;  // timed out: the error word says so
   STAMP(0, 2);
   RingPos rp;
   int buf = 0;
@@ -1934,7 +1977,6 @@ __global__ void __launch_bounds__(kExpertThreads, 1) window_kernel(LayerDev L, W
     combine_all(L, W);
     STAMP(0, 16);
   }
-  if (blockIdx.x == 0 && W.tier.counters) tier_step(W.tier, sp, L.E, m.ring);
 }
 
 // The window kernel on the register-fed path: 16 warps, no producer warp and
@@ -1949,7 +1991,10 @@ __global__ void __launch_bounds__(kConsumerThreads, 1) window_kernel_direct(Laye
   init_cta(C, m, &s_abort);
   for (int i = threadIdx.x; i < 2 * kMaxExperts; i += blockDim.x) (&sp.wcnt[0][0])[i] = 0;
   router_stage<BITS>(L, W, reinterpret_cast<float*>(m.ring));
-  if (!grid_barrier(W, &sp.ok)) return;  // timed out: the error word says so
+  if (!grid_barrier_split(W, &sp.ok, [&] {
+        if (blockIdx.x == 0 && W.tier.counters) tier_round_due(W.tier, L.E, m.ring + kTierScratchOff);
+      }))
+    return;  // timed out: the error word says so
   RingPos rp;
   int buf = 0;
   if (!moe_block<BITS, true>(L, W, C, sp, rg, m, rp, buf)) return;
@@ -1957,7 +2002,6 @@ __global__ void __launch_bounds__(kConsumerThreads, 1) window_kernel_direct(Laye
     if (!grid_barrier(W, &sp.ok) || s_abort) return;
     combine_all(L, W);
   }
-  if (blockIdx.x == 0 && W.tier.counters) tier_step(W.tier, sp, L.E, m.ring);
 }
 
 // A window through n decoder layers in one launch.  Per layer:
@@ -2033,6 +2077,317 @@ __global__ void __launch_bounds__(kExpertThreads, 1)
     }
     if (!grid_barrier(sW, &sp.ok) || s_abort) return;
   }
+}
+
+// ---------------------------------------------------------------------------
+// the output head: logits = W_head RMSNorm(x) for the window's rows, each
+// row's token (greedy or drawn), and each slot's proposal check
+// ---------------------------------------------------------------------------
+
+// Word 0 of Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC 2011) for counter (pos, 0, 0, 0) and key
+// (seed, 0): ten rounds of two 64 x 64 -> 128-bit products of words 0 and 2
+// by the method's two multipliers, the new block (hi(M1 c2) ^ c1 ^ k0,
+// lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)), and the key bumped by its two
+// Weyl increments before every round but the first.
+__device__ __noinline__ unsigned long long philox4x64_word0(unsigned long long pos, unsigned long long seed) {
+  constexpr unsigned long long M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+  constexpr unsigned long long W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+  unsigned long long c0 = pos, c1 = 0, c2 = 0, c3 = 0, k0 = seed, k1 = 0;
+#pragma unroll 1
+  for (int r = 0; r < 10; ++r) {
+    if (r) {
+      k0 += W0;
+      k1 += W1;
+    }
+    const unsigned long long hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
+    const unsigned long long hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
+    c0 = hi1 ^ c1 ^ k0;
+    c1 = lo1;
+    c2 = hi0 ^ c3 ^ k1;
+    c3 = lo0;
+  }
+  return c0;
+}
+
+// The row's uniform in [0, 1): the top 24 bits of the Philox word times 2^-24
+// (exact in fp32).
+__device__ __forceinline__ float row_uniform(unsigned long long pos, unsigned long long seed) {
+  return (float)(philox4x64_word0(pos, seed) >> 40) * 5.9604644775390625e-8f;
+}
+
+// Argmax order: the larger value, then the lower token.
+__device__ __forceinline__ bool better(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
+
+// Probability weight of logit l in a row of maximum M at temperature tau.
+__device__ __forceinline__ float draw_weight(float l, float M, float tau) {
+  return expf(__fdiv_rn(__fsub_rn(l, M), tau));
+}
+
+// Inclusive prefix sums over the block's threads in thread order (warp
+// Kogge-Stone scans, then the warp totals added one after another by thread
+// 0), each thread's result also left in s_incl[tid]; the same arithmetic every
+// time it runs on the same values.  s_w: one float per warp.
+__device__ float block_incl_scan(float v, float* s_incl, float* s_w) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v = __fadd_rn(v, n);
+  }
+  if (lane == 31) s_w[warp] = v;
+  __syncthreads();
+  if (tid == 0) {
+    float run = 0.f;
+    for (int w = 0; w < nw; ++w) {
+      const float tw = s_w[w];
+      s_w[w] = run;
+      run = __fadd_rn(run, tw);
+    }
+  }
+  __syncthreads();
+  const float incl = warp ? __fadd_rn(s_w[warp], v) : v;
+  s_incl[tid] = incl;
+  __syncthreads();
+  return incl;
+}
+
+// This thread's chunk of the CTA's vocabulary slice [v0, v1).
+__device__ __forceinline__ void chunk_of(int v0, int v1, int& a, int& b) {
+  const long long n = v1 - v0;
+  a = v0 + (int)(n * threadIdx.x / blockDim.x);
+  b = v0 + (int)(n * (threadIdx.x + 1) / blockDim.x);
+}
+
+// Sequential sum of the weights of this thread's chunk of row t.
+__device__ __forceinline__ float chunk_weight(const float* lg, int a, int b, float M, float tau) {
+  float s = 0.f;
+  for (int v = a; v < b; ++v) s = __fadd_rn(s, draw_weight(__ldcg(lg + v), M, tau));
+  return s;
+}
+
+// The token of every row from the logits [T][V] (all CTAs; ends with CTA 0
+// writing tokens and the slots' emitted counts).
+//   greedy rows (temperature <= 0): the argmax, ties to the lower token;
+//   sampled rows: u from Philox4x64-10(seed, position); the first token whose
+//   cumulative softmax(logits / temperature) weight exceeds u times the total,
+//   the vocabulary summed slice by slice (CTA order), each slice chunk by
+//   chunk (thread order) and each chunk token by token; should rounding leave
+//   no token above it, the greedy token.
+//   proposal check: a slot's first row (fed < 0) emits its token; each next
+//   row of the slot adds its token while the previous row's token equals the
+//   proposal the row was fed.
+__device__ __noinline__ bool head_select(const WindowBufs& W, const HeadArgs& H, const float* logits, int* s_ok,
+                                         uint8_t* scratch) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = W.T, V = H.V, G = gridDim.x, c = blockIdx.x;
+  float* s_bv = reinterpret_cast<float*>(scratch);               // [2][8]
+  int* s_bi = reinterpret_cast<int*>(s_bv + 2 * kMaxRows);         // [2][8]
+  float* s_M = reinterpret_cast<float*>(s_bi + 2 * kMaxRows);      // [8]
+  float* s_tgt = s_M + kMaxRows;                                   // [8] target within the chosen slice
+  int* s_cs = reinterpret_cast<int*>(s_tgt + kMaxRows);            // [8] the chosen slice
+  float* s_w = reinterpret_cast<float*>(s_cs + kMaxRows);          // [32]
+  float* s_incl = s_w + 32;                                        // [blockDim]
+  int* s_any = reinterpret_cast<int*>(s_incl + blockDim.x);
+  int v0, v1;
+  {
+    v0 = (int)((long long)V * c / G);
+    v1 = (int)((long long)V * (c + 1) / G);
+  }
+  if (tid == 0) {
+    int any = 0;
+    for (int t = 0; t < T; ++t) any |= H.temperature[t] > 0.f ? 1 : 0;
+    *s_any = any;
+  }
+  // A: this slice's maximum and its token, per row (warp w: row w % 8, half w / 8)
+  if (warp < 2 * kMaxRows) {
+    const int t = warp & 7, h = warp >> 3;
+    if (t < T) {
+      const int mid = v0 + (v1 - v0) / 2, lo = h ? mid : v0, hi = h ? v1 : mid;
+      const float* lg = logits + (long long)t * V;
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      bool fin = true;
+      for (int v = lo + lane; v < hi; v += 32) {
+        const float x = __ldcg(lg + v);
+        fin &= isfinite(x);
+        if (x > bv) {
+          bv = x;
+          bi = v;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (!__all_sync(0xffffffffu, fin) && lane == 0) atomicOr(W.err, kErrNonFinite);
+      if (lane == 0) {
+        s_bv[h * kMaxRows + t] = bv;
+        s_bi[h * kMaxRows + t] = bi;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid < T) {
+    float bv = s_bv[tid];
+    int bi = s_bi[tid];
+    if (better(s_bv[kMaxRows + tid], s_bi[kMaxRows + tid], bv, bi)) {
+      bv = s_bv[kMaxRows + tid];
+      bi = s_bi[kMaxRows + tid];
+    }
+    H.part_max[c * kMaxRows + tid] = bv;
+    H.part_arg[c * kMaxRows + tid] = bi;
+  }
+  const bool sampled = *s_any != 0;
+  if (!grid_barrier(W, s_ok)) return false;
+  if (sampled) {
+    // B: every CTA takes each row's maximum; this slice's sum of weights
+    if (tid < T) {
+      float M = -INFINITY;
+#pragma unroll 8
+      for (int q = 0; q < G; ++q) M = fmaxf(M, __ldcg(H.part_max + q * kMaxRows + tid));
+      s_M[tid] = M;
+    }
+    __syncthreads();
+    int a, b;
+    chunk_of(v0, v1, a, b);
+    for (int t = 0; t < T; ++t) {
+      const float tau = H.temperature[t];
+      if (!(tau > 0.f)) continue;
+      const float incl = block_incl_scan(chunk_weight(logits + (long long)t * V, a, b, s_M[t], tau), s_incl, s_w);
+      if (tid == blockDim.x - 1) H.part_sum[c * kMaxRows + t] = incl;
+    }
+    if (!grid_barrier(W, s_ok)) return false;
+    // C: every CTA finds each sampled row's slice: the first whose running
+    // total passes u x (the total); that CTA finds the token inside it
+    if (tid < T) {
+      int cs = -1;
+      float tl = 0.f;
+      if (H.temperature[tid] > 0.f) {
+        float Z = 0.f;
+        for (int q = 0; q < G; ++q) Z = __fadd_rn(Z, __ldcg(H.part_sum + q * kMaxRows + tid));
+        const float tgt = __fmul_rn(row_uniform((unsigned long long)(long long)H.position[tid], H.seed[tid]), Z);
+        float P = 0.f;
+        for (int q = 0; q < G; ++q) {
+          const float Pn = __fadd_rn(P, __ldcg(H.part_sum + q * kMaxRows + tid));
+          if (Pn > tgt) {
+            cs = q;
+            tl = __fsub_rn(tgt, P);
+            break;
+          }
+          P = Pn;
+        }
+      }
+      s_cs[tid] = cs;
+      s_tgt[tid] = tl;
+    }
+    __syncthreads();
+    for (int t = 0; t < T; ++t) {
+      if (s_cs[t] != c) continue;
+      const float tau = H.temperature[t], M = s_M[t], tl = s_tgt[t];
+      const float* lg = logits + (long long)t * V;
+      const float incl = block_incl_scan(chunk_weight(lg, a, b, M, tau), s_incl, s_w);
+      const float excl = tid ? s_incl[tid - 1] : 0.f;
+      const float total = s_incl[blockDim.x - 1];
+      if (tl >= total) {
+        if (tid == 0) H.tokens[t] = v1 - 1;  // rounding: the slice's last token
+      } else if (excl <= tl && tl < incl) {
+        int tok = b - 1;
+        float run = 0.f;
+        for (int v = a; v < b; ++v) {
+          run = __fadd_rn(run, draw_weight(__ldcg(lg + v), M, tau));
+          if (__fadd_rn(excl, run) > tl) {
+            tok = v;
+            break;
+          }
+        }
+        H.tokens[t] = tok;
+      }
+      __syncthreads();
+    }
+    if (!grid_barrier(W, s_ok)) return false;
+  } else if (!grid_barrier(W, s_ok)) {
+    return false;
+  }
+  // final: CTA 0 writes the greedy tokens (and a sampled row's when no slice
+  // passed its target), then each slot's emitted count
+  if (c != 0) return true;
+  if (tid < T) {
+    const bool greedy = !(H.temperature[tid] > 0.f);
+    bool need = greedy;
+    if (!greedy) {
+      float Z = 0.f;
+      for (int q = 0; q < G; ++q) Z = __fadd_rn(Z, __ldcg(H.part_sum + q * kMaxRows + tid));
+      const float tgt = __fmul_rn(row_uniform((unsigned long long)(long long)H.position[tid], H.seed[tid]), Z);
+      need = !(Z > tgt);
+    }
+    if (need) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int q = 0; q < G; ++q) {
+        const float v = __ldcg(H.part_max + q * kMaxRows + tid);
+        const int i = __ldcg(H.part_arg + q * kMaxRows + tid);
+        if (better(v, i, bv, bi)) {
+          bv = v;
+          bi = i;
+        }
+      }
+      H.tokens[tid] = (bi >= 0 && bi < V) ? bi : 0;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    int start = 0, emit = 1;
+    bool ok = true;
+    for (int t = 1; t < T; ++t) {
+      if (H.fed[t] < 0) {  // a new slot
+        H.n_emit[start] = emit;
+        start = t;
+        emit = 1;
+        ok = true;
+      } else {
+        if (ok && __ldcg(H.tokens + t - 1) == H.fed[t]) ++emit;
+        else ok = false;
+        H.n_emit[t] = 0;
+      }
+    }
+    H.n_emit[start] = emit;
+  }
+  return true;
+}
+
+// The head of a window: D0 (1/RMS of each row, the fragments of x / RMS(x);
+// grid barrier), the head GEMV as the dense phase over the V rows of the head
+// matrix (logits to W.q_out; grid barrier), then head_select.
+template <int BITS>
+__global__ void __launch_bounds__(kExpertThreads, 1) head_kernel(LayerDev L, WindowBufs Wp, KernelCfg C, HeadArgs H) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ volatile int s_abort;
+  __shared__ SPlan sp;
+  __shared__ WindowBufs sW;
+  __shared__ float s_rinv[kMaxRows];
+  const Smem m = carve(smem, C);
+  const Ring rg{m.ring, m.full, m.empty, &s_abort};
+  init_cta(C, m, &s_abort);
+  if (threadIdx.x == 0) {
+    sW = Wp;
+    sW.rinv = s_rinv;
+  }
+  __syncthreads();
+  row_rinv(sW.x, sW.T, L.d, s_rinv);
+  write_x_frags<BITS>(L, sW);
+  if (!grid_barrier(sW, &sp.ok)) return;
+  RingPos rp;
+  int buf = 0;
+  dense_phase<BITS, 2>(L, sW, C, sp, rg, m, rp, buf);
+  if (!grid_barrier(sW, &sp.ok) || s_abort) return;
+  head_select(sW, H, sW.q_out, &sp.ok, m.ring);
 }
 
 // ---------------------------------------------------------------------------
@@ -2191,6 +2546,71 @@ cudaError_t launch_window(const LayerDev& L, const WindowBufs& W, const KernelCf
                        : cudaLaunchKernelEx(&cfg, window_kernel_direct<2>, L, W, C);
   if (L.bits == 4) return cudaLaunchKernelEx(&cfg, window_kernel<4>, L, W, C);
   return cudaLaunchKernelEx(&cfg, window_kernel<2>, L, W, C);
+}
+
+// One CTA: the round that is due, if any (strata_tier_read).
+__global__ void __launch_bounds__(kExpertThreads, 1) tier_round_kernel(TierDev Tr, int E) {
+  __shared__ __align__(16) uint8_t scratch[4 * kMaxExperts * 4];
+  tier_round_due(Tr, E, scratch);
+}
+
+cudaError_t launch_tier_round(const TierDev& Tr, int E, cudaStream_t s) {
+  tier_round_kernel<<<1, kExpertThreads, 0, s>>>(Tr, E);
+  return cudaGetLastError();
+}
+
+KernelCfg head_cfg(int d, int bits, int max_rows, int smem_limit) {
+  // the activation buffers of a layer whose inputs are all d wide; phase 2
+  // (the head rows, K = d) cut into ring stages like the dense projections
+  LayerDev L{};
+  L.d = d;
+  L.F = d;
+  L.Fs = 0;
+  L.bits = bits;
+  KernelCfg C = window_cfg(L, max_rows, smem_limit);
+  const int fixed = C.total_bytes - C.nstages * C.stage_bytes;
+  const int ring = smem_limit - fixed;
+  int sb2 = 0;
+  C.ph[2] = phase_cfg(1, bits, d, d, ring / 3, sb2);
+  C.stage_bytes = sb2;
+  const int st = sb2 > 0 ? ring / sb2 : 0;
+  C.nstages = st > kMaxStages ? kMaxStages : st;
+  C.total_bytes = C.nstages * C.stage_bytes + fixed;
+  C.direct = 0;
+  return C;
+}
+
+static const void* head_fn(int bits) {
+  return bits == 4 ? (const void*)head_kernel<4> : (const void*)head_kernel<2>;
+}
+
+cudaError_t head_set_attrs(int bits, int smem_bytes) {
+  return cudaFuncSetAttribute(head_fn(bits), cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+}
+
+int head_blocks_per_sm(int bits, int smem_bytes) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, head_fn(bits), kExpertThreads, smem_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+cudaError_t launch_head(const LayerDev& L, const WindowBufs& W, const KernelCfg& C, const HeadArgs& H, int grid,
+                        cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kExpertThreads);
+  cfg.dynamicSmemBytes = C.total_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (L.bits == 4) return cudaLaunchKernelEx(&cfg, head_kernel<4>, L, W, C, H);
+  return cudaLaunchKernelEx(&cfg, head_kernel<2>, L, W, C, H);
 }
 
 static const void* stack_fn(int bits) {

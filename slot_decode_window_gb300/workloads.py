@@ -247,6 +247,19 @@ def make_dense_layer(wl: Workload, seed: int, layer: int, device: str) -> DenseL
                       make_qmat(1, d, qd, b, B, [sd(_T_O)], device))
 
 
+# The output head of the 48-layer stack's model shape: d = 2048 and a
+# vocabulary of 151,936 tokens (a reading: the pages name no vocabulary; this is
+# the vocabulary of the model family whose layer shapes the stack workload
+# has), 4-bit/32 blocks like the dense weights.
+HEAD_VOCAB = 151936
+_T_HEAD = 12
+
+
+def make_head(vocab: int, hidden: int, bits: int, block: int, seed: int, cfg_id: int, device: str) -> QMat:
+    """A head weight [1][vocab][hidden] in the block format, N(0, 0.02) before quantization."""
+    return make_qmat(1, vocab, hidden, bits, block, [derive_seed(seed, cfg_id, 0, _T_HEAD, 0)], device)
+
+
 AcceptFn = Callable[[np.ndarray], bool]
 
 

@@ -212,3 +212,23 @@ def test_tier_create_rejects_a_bad_initial_list_on_host(lib, initial):
 def test_tier_calls_accept_null(lib):
     assert B.strata_tier_destroy(None) == B.STRATA_OK
     assert B.strata_window_set_tier(None, None) == B.STRATA_EINVAL
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(hidden=0), B.STRATA_EINVAL), (dict(vocab=0), B.STRATA_EINVAL), (dict(max_rows=9), B.STRATA_EINVAL),
+    (dict(bits=3), B.STRATA_EUNSUPPORTED), (dict(vocab=1000), B.STRATA_EUNSUPPORTED),
+    (dict(hidden=96), B.STRATA_EUNSUPPORTED), (dict(bits=2, block=16, hidden=192), B.STRATA_EUNSUPPORTED),
+])
+def test_head_create_rejects_bad_desc_on_host(lib, kw, status):
+    base = dict(hidden=256, vocab=4096, bits=4, block=32, max_rows=8)
+    base.update(kw)
+    q = B.strata_qmat(0x1000, 0x1000, 0x1000)
+    st, h = B.strata_head_create(B.strata_head_desc(**base), q)
+    assert st == status and h is None
+
+
+def test_head_create_rejects_null_weight_pointers(lib):
+    q = B.strata_qmat(0x1000, None, 0x1000)
+    st, h = B.strata_head_create(B.strata_head_desc(256, 4096, 4, 32, 8), q)
+    assert st == B.STRATA_EINVAL and h is None
+    assert B.strata_head_destroy(None) == B.STRATA_OK
