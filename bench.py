@@ -49,6 +49,7 @@ def parse():
     p.add_argument("--sweep-steps", type=int, default=500)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-stack", action="store_true", help="skip the 48-layer stack measurement")
+    p.add_argument("--no-head", action="store_true", help="skip the output-head measurement")
     p.add_argument("--no-workloads", action="store_true", help="skip the zipf and lowbit layer measurements")
     p.add_argument("--stack-steps", type=int, default=30)
     p.add_argument("--stack-layers", type=int, default=2, help="layers of the stack in --mode stack")
@@ -506,6 +507,9 @@ def run_ours(args, rank, world, local_rank):
     # the adaptive tier's bookkeeping attached (counters every window, a round every 4)
     tier = measure_tier(win, X[T], Y[:T], T, flush, min(args.steps, 300))
 
+    # the output head of the stack model's shape (d 2048, V 151,936, 4-bit), T = 8
+    head = None if args.no_head else measure_head(dev, flush, peak)
+
     # end to end through host buffers
     xh = torch.empty(N_WINDOWS, T, d, dtype=torch.float32).pin_memory()
     xh.copy_(X[T].cpu())
@@ -566,7 +570,7 @@ def run_ours(args, rank, world, local_rank):
             "config": bench_config(wl, T, world),
             "arith": "codes -> exact fp16 integers; mma.sync f16 x (fp16 hi + lo activations), fp32 accumulate; "
                      "fp32 router, softmax, SwiGLU, combine",
-            "roofline": roofline, "sweep": sweep, "graph": graph, "tier": tier, "workloads": workloads,
+            "roofline": roofline, "sweep": sweep, "graph": graph, "tier": tier, "head": head, "workloads": workloads,
             "stack48": stack, "e2e": e2e,
             "clocks": clocks,
             "cpu_baseline": cpu, "cpu_baselines": cpu_all,
@@ -578,6 +582,48 @@ def run_ours(args, rank, world, local_rank):
         }
         print(json.dumps(line), flush=True)
     win.close()
+
+
+def measure_head(dev, flush, peak, steps=200):
+    """The output head at the 48-layer stack's model shape (d 2048, V 151,936,
+    4-bit/32): a T = 8 window of 4 slots x (token, proposal), half greedy and
+    half sampled rows; kernel time from profiling-mode events, L2 flushed
+    before each window.  Algorithmic bytes: the head's block bytes, the rows
+    of x, and the logits written once and read by the draw."""
+    import numpy as np
+    import torch
+    from slot_decode_window_gb300 import binding, workloads as wlm
+    d, V, T = 2048, wlm.HEAD_VOCAB, 8
+    W = wlm.make_head(V, d, 4, 32, seed=0, cfg_id=4, device=str(dev))
+    head = binding.Head(W, max_rows=8)
+    del W
+    torch.cuda.empty_cache()
+    hb = head.head_bytes()
+    xs = torch.from_numpy(np.random.default_rng(0).standard_normal((16, T, d)).astype(np.float32)).to(dev)
+    pos = torch.arange(100, 100 + T, dtype=torch.int32, device=dev)
+    seed = torch.full((T,), 12345, dtype=torch.int64, device=dev)
+    temp = torch.tensor([0.0, 0.0, 0.7, 0.7, 0.0, 0.0, 1.0, 1.0], device=dev)
+    fed = torch.tensor([-1, 0, -1, 0, -1, 0, -1, 0], dtype=torch.int32, device=dev)
+    for i in range(5):
+        head.forward(xs[i % 16], pos, seed, temp, fed)
+    head.set_profiling(True)
+    ms = []
+    for i in range(steps):
+        flush_and_hold(flush)
+        head.forward(xs[i % 16], pos, seed, temp, fed)
+        ms.append(head.timings())
+    head.set_profiling(False)
+    head.sync()
+    head.close()
+    nbytes = hb + T * d * 4 + 2 * T * V * 4
+    mean_s = statistics.mean(ms) / 1e3
+    q10, q50, q90 = percentiles(ms)
+    return {"workload": "output head d 2048, V 151,936, 4-bit/32, T = 8 (4 slots x (token, proposal)), "
+                        "greedy and sampled rows, proposal check",
+            "kernel": "head_kernel<4> (RMSNorm, head GEMV, draw, proposal check; one cooperative launch)",
+            "us_per_window_mean": 1e6 * mean_s, "us_per_window_p10": 1e3 * q10, "us_per_window_median": 1e3 * q50,
+            "us_per_window_p90": 1e3 * q90, "algorithmic_bytes": nbytes, "achieved_GBps": nbytes / mean_s / 1e9,
+            "frac_of_measured_hbm": nbytes / mean_s / 1e9 / peak, "rows_per_s": T / mean_s}
 
 
 def measure_tier(win, X, Y, T, flush, steps):

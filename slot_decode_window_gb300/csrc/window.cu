@@ -169,9 +169,13 @@ __device__ __forceinline__ KWords<BITS> kwords_smem(const uint8_t* __restrict__ 
   return kw;
 }
 
+// acc: the hi parts' columns (paired: every column); acc2: the lo parts'
+// columns in the two-set layout (unused when paired).  The hi and lo products
+// of a row run in separate MMA chains and accumulators in both layouts, so a
+// row's arithmetic does not depend on how many rows share its group.
 template <int BITS, bool PAIRED>
 __device__ __forceinline__ void kstep_compute(const KWords<BITS>& kw, const __half* __restrict__ bk, int bm_set,
-                                              int lane, float (&acc)[4]) {
+                                              int lane, float (&acc)[4], float (&acc2)[4]) {
   const float z4[4] = {0.f, 0.f, 0.f, 0.f};
   if constexpr (BITS == 4) {
     const uint4 bA = *reinterpret_cast<const uint4*>(bk);
@@ -190,23 +194,28 @@ __device__ __forceinline__ void kstep_compute(const KWords<BITS>& kw, const __ha
       const uint32_t wg = blk ? cw.z : cw.x, w8 = blk ? cw.w : cw.y;
       const uint32_t wg2 = wg >> 8, w82 = w8 >> 8;
       const uint4 b = blk ? bB : bA;
+      const float sgv = blk ? sg.y : sg.x, s8v = blk ? s8.y : s8.x;
       float d[4];
       mma16816(d, dq_pair(wg, 0x000F000Fu), dq_pair(w8, 0x000F000Fu), dq_pair(wg2, 0x000F000Fu),
                dq_pair(w82, 0x000F000Fu), b.x, b.y, z4);
       mma16816(d, dq_pair(wg, 0x00F000F0u), dq_pair(w8, 0x00F000F0u), dq_pair(wg2, 0x00F000F0u),
                dq_pair(w82, 0x00F000F0u), b.z, b.w, d);
-      if constexpr (!PAIRED) {
-        const uint4 l = blk ? lB : lA;
-        mma16816(d, dq_pair(wg, 0x000F000Fu), dq_pair(w8, 0x000F000Fu), dq_pair(wg2, 0x000F000Fu),
-                 dq_pair(w82, 0x000F000Fu), l.x, l.y, d);
-        mma16816(d, dq_pair(wg, 0x00F000F0u), dq_pair(w8, 0x00F000F0u), dq_pair(wg2, 0x00F000F0u),
-                 dq_pair(w82, 0x00F000F0u), l.z, l.w, d);
-      }
-      const float sgv = blk ? sg.y : sg.x, s8v = blk ? s8.y : s8.x;
       acc[0] = fmaf(sgv, d[0], acc[0]);
       acc[1] = fmaf(sgv, d[1], acc[1]);
       acc[2] = fmaf(s8v, d[2], acc[2]);
       acc[3] = fmaf(s8v, d[3], acc[3]);
+      if constexpr (!PAIRED) {
+        const uint4 l = blk ? lB : lA;
+        float e[4];
+        mma16816(e, dq_pair(wg, 0x000F000Fu), dq_pair(w8, 0x000F000Fu), dq_pair(wg2, 0x000F000Fu),
+                 dq_pair(w82, 0x000F000Fu), l.x, l.y, z4);
+        mma16816(e, dq_pair(wg, 0x00F000F0u), dq_pair(w8, 0x00F000F0u), dq_pair(wg2, 0x00F000F0u),
+                 dq_pair(w82, 0x00F000F0u), l.z, l.w, e);
+        acc2[0] = fmaf(sgv, e[0], acc2[0]);
+        acc2[1] = fmaf(sgv, e[1], acc2[1]);
+        acc2[2] = fmaf(s8v, e[2], acc2[2]);
+        acc2[3] = fmaf(s8v, e[3], acc2[3]);
+      }
     }
   } else {
     const uint4 cw = kw.cw, sa = kw.sa, sb = kw.sb;
@@ -224,22 +233,32 @@ __device__ __forceinline__ void kstep_compute(const KWords<BITS>& kw, const __ha
       float d[4];
       mma16816(d, dq_pair(w, 0x00030003u), dq_pair(w2, 0x00030003u), dq_pair(w, 0x000C000Cu),
                dq_pair(w2, 0x000C000Cu), b.x, b.y, z4);
-      if constexpr (!PAIRED)
-        mma16816(d, dq_pair(w, 0x00030003u), dq_pair(w2, 0x00030003u), dq_pair(w, 0x000C000Cu),
-                 dq_pair(w2, 0x000C000Cu), l.x, l.y, d);
       acc[0] = fmaf(sgp.x, d[0], acc[0]);
       acc[1] = fmaf(sgp.x, d[1], acc[1]);
       acc[2] = fmaf(s8p.x, d[2], acc[2]);
       acc[3] = fmaf(s8p.x, d[3], acc[3]);
+      if constexpr (!PAIRED) {
+        mma16816(d, dq_pair(w, 0x00030003u), dq_pair(w2, 0x00030003u), dq_pair(w, 0x000C000Cu),
+                 dq_pair(w2, 0x000C000Cu), l.x, l.y, z4);
+        acc2[0] = fmaf(sgp.x, d[0], acc2[0]);
+        acc2[1] = fmaf(sgp.x, d[1], acc2[1]);
+        acc2[2] = fmaf(s8p.x, d[2], acc2[2]);
+        acc2[3] = fmaf(s8p.x, d[3], acc2[3]);
+      }
       mma16816(d, dq_pair(w, 0x00300030u), dq_pair(w2, 0x00300030u), dq_pair(w, 0x00C000C0u),
                dq_pair(w2, 0x00C000C0u), b.z, b.w, z4);
-      if constexpr (!PAIRED)
-        mma16816(d, dq_pair(w, 0x00300030u), dq_pair(w2, 0x00300030u), dq_pair(w, 0x00C000C0u),
-                 dq_pair(w2, 0x00C000C0u), l.z, l.w, d);
       acc[0] = fmaf(sgp.y, d[0], acc[0]);
       acc[1] = fmaf(sgp.y, d[1], acc[1]);
       acc[2] = fmaf(s8p.y, d[2], acc[2]);
       acc[3] = fmaf(s8p.y, d[3], acc[3]);
+      if constexpr (!PAIRED) {
+        mma16816(d, dq_pair(w, 0x00300030u), dq_pair(w2, 0x00300030u), dq_pair(w, 0x00C000C0u),
+                 dq_pair(w2, 0x00C000C0u), l.z, l.w, z4);
+        acc2[0] = fmaf(sgp.y, d[0], acc2[0]);
+        acc2[1] = fmaf(sgp.y, d[1], acc2[1]);
+        acc2[2] = fmaf(s8p.y, d[2], acc2[2]);
+        acc2[3] = fmaf(s8p.y, d[3], acc2[3]);
+      }
     }
   }
 }
@@ -247,8 +266,29 @@ __device__ __forceinline__ void kstep_compute(const KWords<BITS>& kw, const __ha
 // One k-step of one sub-tile from a staged chunk in shared memory.
 template <int BITS, bool PAIRED>
 __device__ __forceinline__ void kstep_mma(const uint8_t* __restrict__ ch, const __half* __restrict__ bk, int bm_set,
-                                          int lane, float (&acc)[4]) {
-  kstep_compute<BITS, PAIRED>(kwords_smem<BITS>(ch, lane), bk, bm_set, lane, acc);
+                                          int lane, float (&acc)[4], float (&acc2)[4]) {
+  kstep_compute<BITS, PAIRED>(kwords_smem<BITS>(ch, lane), bk, bm_set, lane, acc, acc2);
+}
+
+// A warp's partial outputs of one task for the reduction buffer: per
+// output, fma(acc, 2^24, accm) of its hi part plus that of its lo part.
+// Paired: columns (2q, 2q + 1) of a lane are row q's hi and lo parts, so
+// the lane's two outputs (weight rows g, g + 8) land in .x and .z; two-set:
+// the lane's four outputs (rows 2q, 2q + 1 at g, g + 8) in .x .y .z .w.
+template <bool PAIRED>
+__device__ __forceinline__ float4 partials(const float (&acc)[4], const float (&accm)[4], const float (&acc2)[4],
+                                           const float (&accm2)[4]) {
+  float h[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = fmaf(acc[i], kDqUnscale, accm[i]);
+  if constexpr (PAIRED) {
+    return make_float4(h[0] + h[1], 0.f, h[2] + h[3], 0.f);
+  } else {
+    float l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) l[i] = fmaf(acc2[i], kDqUnscale, accm2[i]);
+    return make_float4(h[0] + l[0], h[1] + l[1], h[2] + l[2], h[3] + l[3]);
+  }
 }
 
 // This warp's share of one staged chunk of its sub-tile: k-steps [k0, k1)
@@ -261,7 +301,8 @@ template <int BITS, bool PAIRED, bool VMAP = false>
 __device__ __forceinline__ void chunk_mma(const uint8_t* __restrict__ sub, int mins_off, int ks_base, int k0, int k1,
                                           int mk_base, int m0, int m1, const __half* __restrict__ bm,
                                           const __half* __restrict__ bs, int bm_set, int bs_set, int lane_b, int lane,
-                                          float (&acc)[4], float (&accm)[4], int kph = 0, int kpg = 0) {
+                                          float (&acc)[4], float (&accm)[4], float (&acc2)[4], float (&accm2)[4],
+                                          int kph = 0, int kpg = 0) {
   constexpr int S = Fmt<BITS>::kBHalves;
   const uint8_t* a = sub + k0 * Fmt<BITS>::kChunk;
   const __half* bk = bm + (ks_base + k0) * 32 * S + lane_b * 8;
@@ -271,7 +312,7 @@ __device__ __forceinline__ void chunk_mma(const uint8_t* __restrict__ sub, int m
       const int ks = ks_base + kl;
       bk = bm + (((ks >> kpg) << kph) + (ks & ((1 << kph) - 1))) * 32 * S + lane_b * 8;
     }
-    kstep_mma<BITS, PAIRED>(a, bk, bm_set, lane, acc);
+    kstep_mma<BITS, PAIRED>(a, bk, bm_set, lane, acc, acc2);
     a += Fmt<BITS>::kChunk;
     bk += 32 * S;
   }
@@ -283,7 +324,7 @@ __device__ __forceinline__ void chunk_mma(const uint8_t* __restrict__ sub, int m
     mma16816(accm, am.x, am.y, am.z, am.w, b.x, b.y, accm);
     if constexpr (!PAIRED) {
       const uint2 l = *reinterpret_cast<const uint2*>(sp + bs_set);
-      mma16816(accm, am.x, am.y, am.z, am.w, l.x, l.y, accm);
+      mma16816(accm2, am.x, am.y, am.z, am.w, l.x, l.y, accm2);
     }
     am_p += 512;
     sp += 128;
@@ -519,10 +560,10 @@ __device__ __noinline__ void router_stage(const LayerDev& L, const WindowBufs& W
 // All CTAs arrive; thread 0 waits (bounded) until every CTA of this window has.
 // The counter only grows: the window's target is the next multiple of the grid
 // (plus W.bar_extra, which is 0 except in tests that make the wait run out).
-// grid_barrier_split arrives, runs `between` with all threads of the CTA, and
-// then waits.
+// grid_barrier_split arrives, runs `between` with all threads of the CTA when
+// `run` (the same for every thread of the CTA), and then waits.
 template <typename F>
-__device__ bool grid_barrier_split(const WindowBufs& W, int* s_ok, F between) {
+__device__ bool grid_barrier_split(const WindowBufs& W, int* s_ok, bool run, F between) {
   __shared__ unsigned long long s_target;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -531,8 +572,10 @@ __device__ bool grid_barrier_split(const WindowBufs& W, int* s_ok, F between) {
     const unsigned long long old = atomicAdd(W.gbar, 1ull);
     s_target = (old / n + 1) * n + (unsigned long long)W.bar_extra;
   }
-  between();
-  __syncthreads();
+  if (run) {
+    between();
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
     const unsigned long long target = s_target;
     const long long t0 = clock64();
@@ -553,7 +596,7 @@ __device__ bool grid_barrier_split(const WindowBufs& W, int* s_ok, F between) {
 }
 
 __device__ __forceinline__ bool grid_barrier(const WindowBufs& W, int* s_ok) {
-  return grid_barrier_split(W, s_ok, [] {});
+  return grid_barrier_split(W, s_ok, false, [] {});
 }
 
 // Row t (warp t; lane holds experts lane + 32 i): logits as the column-chunk
@@ -1202,12 +1245,13 @@ __device__ bool produce(const LayerDev& L, const WindowBufs& W, const KernelCfg&
 // ---------------------------------------------------------------------------
 // consumers: one phase's tasks (all 16 consumer warps)
 // ---------------------------------------------------------------------------
-// One output of an accumulator fragment: element idx (paired: the hi + lo
-// columns idx and idx + 1).  Selects, not an indexed array, so the fragment
-// stays in registers.
+// One output of a warp's partials (see partials): element idx, whose low
+// bit is 0 in the paired layout.  Selects, not an indexed array, so the
+// fragment stays in registers.
 __device__ __forceinline__ float frag_pick(const float4 a, int idx, bool paired) {
+  (void)paired;
   const float lo = (idx & 2) ? a.z : a.x, hi = (idx & 2) ? a.w : a.y;
-  return paired ? lo + hi : ((idx & 1) ? hi : lo);
+  return (idx & 1) ? hi : lo;
 }
 
 // Group state of the consumer loop: rows of the current group and their MMA
@@ -1387,6 +1431,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
     if (tk.group != gs.cur) enter_group<BITS, PHASE>(L, W, C, sp, tk, K, rg.abort_flag, bm, bs, gs);
     const int kv = (PHASE == 1 && tk.shared) ? 1 : 0;
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc2[4] = {0.f, 0.f, 0.f, 0.f}, accm2[4] = {0.f, 0.f, 0.f, 0.f};
     if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 0);
     for (int ch = 0; ch < P.nchunks; ++ch) {
       const int ks0 = P.cks[kv][ch], ks1 = P.cks[kv][ch + 1];
@@ -1401,10 +1446,12 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
         constexpr bool kVmap = PHASE == 3;
         if (gs.paired)
           chunk_mma<BITS, true, kVmap>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
-                                       C.bsum_halves, gs.lane_b, lane, acc, accm, L.kph_log2, L.kpg_log2);
+                                       C.bsum_halves, gs.lane_b, lane, acc, accm, acc2, accm2, L.kph_log2,
+                                       L.kpg_log2);
         else
           chunk_mma<BITS, false, kVmap>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
-                                        C.bsum_halves, gs.lane_b, lane, acc, accm, L.kph_log2, L.kpg_log2);
+                                        C.bsum_halves, gs.lane_b, lane, acc, accm, acc2, accm2, L.kph_log2,
+                                        L.kpg_log2);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&rg.empty[stage]);
@@ -1412,8 +1459,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
     }
     if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 2);
     float4* rb = red + buf * (kConsumerWarps * 32);
-    rb[warp * 32 + lane] = make_float4(fmaf(acc[0], kDqUnscale, accm[0]), fmaf(acc[1], kDqUnscale, accm[1]),
-                                       fmaf(acc[2], kDqUnscale, accm[2]), fmaf(acc[3], kDqUnscale, accm[3]));
+    rb[warp * 32 + lane] = gs.paired ? partials<true>(acc, accm, acc2, accm2) : partials<false>(acc, accm, acc2, accm2);
     consumer_sync();  // all 16 warps: the ring path's warps stay in step
     if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 3);
 
@@ -1590,6 +1636,7 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
       }
       const ItemRange r = item_range<BITS, NS>(K, kg);
       float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc2[4] = {0.f, 0.f, 0.f, 0.f}, accm2[4] = {0.f, 0.f, 0.f, 0.f};
       const __half* bk = bm + r.k0 * 32 * S + gs.lane_b * 8;
       const __half* bsm = bs + r.m0 * 128 + gs.lane_b * 4;
       // refill the slot just used with the stream's next item, then move on
@@ -1606,7 +1653,7 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
         for (int ci = 0; ci < r.nk; ++ci) {
           cp_async_wait_group<kDepth - 1>();
           __syncwarp();
-          kstep_mma<BITS, true>(it, bk, C.bmain_halves, lane, acc);
+          kstep_mma<BITS, true>(it, bk, C.bmain_halves, lane, acc, acc2);
           bk += 32 * S;
           next_slot();
         }
@@ -1614,7 +1661,7 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
         for (int ci = 0; ci < r.nk; ++ci) {
           cp_async_wait_group<kDepth - 1>();
           __syncwarp();
-          kstep_mma<BITS, false>(it, bk, C.bmain_halves, lane, acc);
+          kstep_mma<BITS, false>(it, bk, C.bmain_halves, lane, acc, acc2);
           bk += 32 * S;
           next_slot();
         }
@@ -1627,14 +1674,14 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
         mma16816(accm, am.x, am.y, am.z, am.w, b.x, b.y, accm);
         if (!gs.paired) {
           const uint2 l = *reinterpret_cast<const uint2*>(bsm + C.bsum_halves);
-          mma16816(accm, am.x, am.y, am.z, am.w, l.x, l.y, accm);
+          mma16816(accm2, am.x, am.y, am.z, am.w, l.x, l.y, accm2);
         }
         bsm += 128;
         next_slot();
       }
       float4* rb = red + buf * (kConsumerWarps * 32);
-      rb[warp * 32 + lane] = make_float4(fmaf(acc[0], kDqUnscale, accm[0]), fmaf(acc[1], kDqUnscale, accm[1]),
-                                         fmaf(acc[2], kDqUnscale, accm[2]), fmaf(acc[3], kDqUnscale, accm[3]));
+      rb[warp * 32 + lane] =
+          gs.paired ? partials<true>(acc, accm, acc2, accm2) : partials<false>(acc, accm, acc2, accm2);
       og.sync();
       {
         constexpr int kGT = OutGroup<PHASE, NS>::kThreads;
@@ -1822,26 +1869,29 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
     return false;
   }
   const bool has_shared = L.Fs > 0;
+  // Task widths depend on the layer shape only, never on the window's
+  // routing: a task's sub-tile count fixes how its K is split over the warps
+  // (and so the order of a row's fp32 sums), and a row must get the same bits
+  // whatever other rows share its window (the Strata docs, "BATCHING.md",
+  // section "Exactness": a batch row's arithmetic is the single-token
+  // window's).
   if (warp == 0) {
-    // gate/up: 2 row tiles per task when that still leaves >= 3 tasks per CTA
+    // gate/up: 2 row tiles per task (the gate and up sub-tiles of each)
     PhaseTasks& p0 = sp.pt[0];
     const int tiles_e = L.F / 16, tiles_s = has_shared ? L.Fs / 16 : 0;
-    const long long all0 = tiles_s + (long long)nd * tiles_e;
-    p0.mt = (C.ph[0].max_sub >= 4 && tiles_e % 2 == 0 && tiles_s % 2 == 0 && all0 / 2 >= 3LL * gridDim.x) ? 2 : 1;
+    p0.mt = (C.ph[0].max_sub >= 4 && tiles_e % 2 == 0 && tiles_s % 2 == 0) ? 2 : 1;
     p0.ntask_s = tiles_s / p0.mt;
     p0.ntask_e = tiles_e / p0.mt;
     split_tasks(W, sp, has_shared, p0, lane);
   } else if (warp == 1) {
-    // down: as many row tiles per task (up to 4) as keep >= 1 task per CTA;
-    // with few rows a down task is short, and its fixed cost (wait, sync,
-    // epilogue) outweighs the finer balance of narrower tasks
+    // down: as many row tiles per task (up to 4) as the stage plan allows and
+    // the d / 16 row tiles divide into (a down task is short, and its fixed
+    // cost outweighs finer balance); the warp-streamed path's plan allows 4,
+    // so every warp there has a k-step of each task
     PhaseTasks& p1 = sp.pt[1];
     const int tiles_g = L.d / 16;
-    const long long all1 = (long long)((has_shared ? 1 : 0) + nd) * tiles_g;
     int mt = C.ph[1].max_sub;
-    // (the register-fed path keeps >= 2 tiles per task: every warp then has
-    // at least one k-step of each task)
-    while (mt > (DIRECT ? 2 : 1) && (tiles_g % mt != 0 || all1 / mt < (long long)gridDim.x)) mt >>= 1;
+    while (mt > 1 && tiles_g % mt != 0) mt >>= 1;
     p1.mt = mt;
     p1.ntask_s = has_shared ? tiles_g / mt : 0;
     p1.ntask_e = tiles_g / mt;
@@ -1963,9 +2013,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) window_kernel(LayerDev L, W
   __syncthreads();
   STAMP(0, 19);
 #endif
-  if (!grid_barrier_split(W, &sp.ok, [&] {
-        if (blockIdx.x == 0 && W.tier.counters) tier_round_due(W.tier, L.E, m.ring + kTierScratchOff);
-      }))
+  if (!grid_barrier_split(W, &sp.ok, blockIdx.x == 0 && W.tier.counters != nullptr,
+                          [&] { tier_round_due(W.tier, L.E, m.ring + kTierScratchOff); }))
     return;  // timed out: the error word says so
   STAMP(0, 2);
   RingPos rp;
@@ -1991,9 +2040,8 @@ __global__ void __launch_bounds__(kConsumerThreads, 1) window_kernel_direct(Laye
   init_cta(C, m, &s_abort);
   for (int i = threadIdx.x; i < 2 * kMaxExperts; i += blockDim.x) (&sp.wcnt[0][0])[i] = 0;
   router_stage<BITS>(L, W, reinterpret_cast<float*>(m.ring));
-  if (!grid_barrier_split(W, &sp.ok, [&] {
-        if (blockIdx.x == 0 && W.tier.counters) tier_round_due(W.tier, L.E, m.ring + kTierScratchOff);
-      }))
+  if (!grid_barrier_split(W, &sp.ok, blockIdx.x == 0 && W.tier.counters != nullptr,
+                          [&] { tier_round_due(W.tier, L.E, m.ring + kTierScratchOff); }))
     return;  // timed out: the error word says so
   RingPos rp;
   int buf = 0;
