@@ -553,13 +553,13 @@ def run_ours(args, rank, world, local_rank):
     cpu = cpu_all = None
     if want_cpu:
         cpu_all = cpu_baselines(cpu_jobs)
-        head = cpu_all[args.workload]
-        cpu = {"value": head["all_cores"]["rows_per_s"], "unit": UNIT, "cores": head["all_cores"]["threads"],
+        own = cpu_all[args.workload]
+        cpu = {"value": own["all_cores"]["rows_per_s"], "unit": UNIT, "cores": own["all_cores"]["threads"],
                "kind": "oracle",
-               "sample": f"{head['windows']} windows of T={T} of the bench's inputs, each window evaluated row by "
-                         f"row by the fp64 oracle in a spawned process with {head['all_cores']['threads']} BLAS "
-                         f"threads, {head['all_cores']['seconds']:.1f} s",
-               "one_thread": head["one_thread"]}
+               "sample": f"{own['windows']} windows of T={T} of the bench's inputs, each window evaluated row by "
+                         f"row by the fp64 oracle in a spawned process with {own['all_cores']['threads']} BLAS "
+                         f"threads, {own['all_cores']['seconds']:.1f} s",
+               "one_thread": own["one_thread"]}
     p10, p50, p90 = percentiles(ms)
 
     if rank == 0:

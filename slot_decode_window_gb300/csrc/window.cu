@@ -169,13 +169,32 @@ __device__ __forceinline__ KWords<BITS> kwords_smem(const uint8_t* __restrict__ 
   return kw;
 }
 
-// acc: the hi parts' columns (paired: every column); acc2: the lo parts'
-// columns in the two-set layout (unused when paired).  The hi and lo products
-// of a row run in separate MMA chains and accumulators in both layouts, so a
-// row's arithmetic does not depend on how many rows share its group.
+// A row's hi and lo parts run in separate MMA chains in both column layouts:
+// paired, columns (2q, 2q + 1) are row q's (hi, lo), so a lane's d[0], d[1]
+// (weight row g) and d[2], d[3] (row g + 8) pair up in place; two-set, the
+// hi parts are one set of columns (d) and the lo parts the other (e).  Each
+// block's t = d_hi + d_lo is then scaled into the accumulator, so a row's
+// arithmetic is the same whether its group has 1 row or 8: the Strata docs
+// ("BATCHING.md", section "Exactness") make a batch row's arithmetic the
+// single-token window's.  acc: paired, [0] and [2] hold weight rows g and
+// g + 8; two-set, [0..3] hold (rows 2q, 2q + 1) x (g, g + 8).
+template <bool PAIRED>
+__device__ __forceinline__ void scale_into(float (&acc)[4], const float (&d)[4], const float (&e)[4], float sg,
+                                           float s8) {
+  if constexpr (PAIRED) {
+    acc[0] = fmaf(sg, d[0] + d[1], acc[0]);
+    acc[2] = fmaf(s8, d[2] + d[3], acc[2]);
+  } else {
+    acc[0] = fmaf(sg, d[0] + e[0], acc[0]);
+    acc[1] = fmaf(sg, d[1] + e[1], acc[1]);
+    acc[2] = fmaf(s8, d[2] + e[2], acc[2]);
+    acc[3] = fmaf(s8, d[3] + e[3], acc[3]);
+  }
+}
+
 template <int BITS, bool PAIRED>
 __device__ __forceinline__ void kstep_compute(const KWords<BITS>& kw, const __half* __restrict__ bk, int bm_set,
-                                              int lane, float (&acc)[4], float (&acc2)[4]) {
+                                              int lane, float (&acc)[4]) {
   const float z4[4] = {0.f, 0.f, 0.f, 0.f};
   if constexpr (BITS == 4) {
     const uint4 bA = *reinterpret_cast<const uint4*>(bk);
@@ -194,28 +213,19 @@ __device__ __forceinline__ void kstep_compute(const KWords<BITS>& kw, const __ha
       const uint32_t wg = blk ? cw.z : cw.x, w8 = blk ? cw.w : cw.y;
       const uint32_t wg2 = wg >> 8, w82 = w8 >> 8;
       const uint4 b = blk ? bB : bA;
-      const float sgv = blk ? sg.y : sg.x, s8v = blk ? s8.y : s8.x;
-      float d[4];
+      float d[4], e[4];
       mma16816(d, dq_pair(wg, 0x000F000Fu), dq_pair(w8, 0x000F000Fu), dq_pair(wg2, 0x000F000Fu),
                dq_pair(w82, 0x000F000Fu), b.x, b.y, z4);
       mma16816(d, dq_pair(wg, 0x00F000F0u), dq_pair(w8, 0x00F000F0u), dq_pair(wg2, 0x00F000F0u),
                dq_pair(w82, 0x00F000F0u), b.z, b.w, d);
-      acc[0] = fmaf(sgv, d[0], acc[0]);
-      acc[1] = fmaf(sgv, d[1], acc[1]);
-      acc[2] = fmaf(s8v, d[2], acc[2]);
-      acc[3] = fmaf(s8v, d[3], acc[3]);
       if constexpr (!PAIRED) {
         const uint4 l = blk ? lB : lA;
-        float e[4];
         mma16816(e, dq_pair(wg, 0x000F000Fu), dq_pair(w8, 0x000F000Fu), dq_pair(wg2, 0x000F000Fu),
                  dq_pair(w82, 0x000F000Fu), l.x, l.y, z4);
         mma16816(e, dq_pair(wg, 0x00F000F0u), dq_pair(w8, 0x00F000F0u), dq_pair(wg2, 0x00F000F0u),
                  dq_pair(w82, 0x00F000F0u), l.z, l.w, e);
-        acc2[0] = fmaf(sgv, e[0], acc2[0]);
-        acc2[1] = fmaf(sgv, e[1], acc2[1]);
-        acc2[2] = fmaf(s8v, e[2], acc2[2]);
-        acc2[3] = fmaf(s8v, e[3], acc2[3]);
       }
+      scale_into<PAIRED>(acc, d, e, blk ? sg.y : sg.x, blk ? s8.y : s8.x);
     }
   } else {
     const uint4 cw = kw.cw, sa = kw.sa, sb = kw.sb;
@@ -230,65 +240,44 @@ __device__ __forceinline__ void kstep_compute(const KWords<BITS>& kw, const __ha
       const uint32_t w = cwv[j], w2 = w >> 8;
       const float2 sgp = __half22float2(*reinterpret_cast<const __half2*>(&sav[j]));
       const float2 s8p = __half22float2(*reinterpret_cast<const __half2*>(&sbv[j]));
-      float d[4];
+      float d[4], e[4];
       mma16816(d, dq_pair(w, 0x00030003u), dq_pair(w2, 0x00030003u), dq_pair(w, 0x000C000Cu),
                dq_pair(w2, 0x000C000Cu), b.x, b.y, z4);
-      acc[0] = fmaf(sgp.x, d[0], acc[0]);
-      acc[1] = fmaf(sgp.x, d[1], acc[1]);
-      acc[2] = fmaf(s8p.x, d[2], acc[2]);
-      acc[3] = fmaf(s8p.x, d[3], acc[3]);
-      if constexpr (!PAIRED) {
-        mma16816(d, dq_pair(w, 0x00030003u), dq_pair(w2, 0x00030003u), dq_pair(w, 0x000C000Cu),
+      if constexpr (!PAIRED)
+        mma16816(e, dq_pair(w, 0x00030003u), dq_pair(w2, 0x00030003u), dq_pair(w, 0x000C000Cu),
                  dq_pair(w2, 0x000C000Cu), l.x, l.y, z4);
-        acc2[0] = fmaf(sgp.x, d[0], acc2[0]);
-        acc2[1] = fmaf(sgp.x, d[1], acc2[1]);
-        acc2[2] = fmaf(s8p.x, d[2], acc2[2]);
-        acc2[3] = fmaf(s8p.x, d[3], acc2[3]);
-      }
+      scale_into<PAIRED>(acc, d, e, sgp.x, s8p.x);
       mma16816(d, dq_pair(w, 0x00300030u), dq_pair(w2, 0x00300030u), dq_pair(w, 0x00C000C0u),
                dq_pair(w2, 0x00C000C0u), b.z, b.w, z4);
-      acc[0] = fmaf(sgp.y, d[0], acc[0]);
-      acc[1] = fmaf(sgp.y, d[1], acc[1]);
-      acc[2] = fmaf(s8p.y, d[2], acc[2]);
-      acc[3] = fmaf(s8p.y, d[3], acc[3]);
-      if constexpr (!PAIRED) {
-        mma16816(d, dq_pair(w, 0x00300030u), dq_pair(w2, 0x00300030u), dq_pair(w, 0x00C000C0u),
+      if constexpr (!PAIRED)
+        mma16816(e, dq_pair(w, 0x00300030u), dq_pair(w2, 0x00300030u), dq_pair(w, 0x00C000C0u),
                  dq_pair(w2, 0x00C000C0u), l.z, l.w, z4);
-        acc2[0] = fmaf(sgp.y, d[0], acc2[0]);
-        acc2[1] = fmaf(sgp.y, d[1], acc2[1]);
-        acc2[2] = fmaf(s8p.y, d[2], acc2[2]);
-        acc2[3] = fmaf(s8p.y, d[3], acc2[3]);
-      }
+      scale_into<PAIRED>(acc, d, e, sgp.y, s8p.y);
     }
+  }
+}
+
+// A warp's partial outputs of one task for the reduction buffer: per output
+// fma(acc, 2^24, m_hi + m_lo), the min term's hi and lo chains (paired: accm
+// columns 2q, 2q + 1; two-set: accm and accm2) added first.  Paired: the
+// lane's two outputs (weight rows g, g + 8) land in .x and .z; two-set: its
+// four outputs (rows 2q, 2q + 1 at g, g + 8) in .x .y .z .w.
+template <bool PAIRED>
+__device__ __forceinline__ float4 partials(const float (&acc)[4], const float (&accm)[4], const float (&accm2)[4]) {
+  if constexpr (PAIRED) {
+    return make_float4(fmaf(acc[0], kDqUnscale, accm[0] + accm[1]), 0.f,
+                       fmaf(acc[2], kDqUnscale, accm[2] + accm[3]), 0.f);
+  } else {
+    return make_float4(fmaf(acc[0], kDqUnscale, accm[0] + accm2[0]), fmaf(acc[1], kDqUnscale, accm[1] + accm2[1]),
+                       fmaf(acc[2], kDqUnscale, accm[2] + accm2[2]), fmaf(acc[3], kDqUnscale, accm[3] + accm2[3]));
   }
 }
 
 // One k-step of one sub-tile from a staged chunk in shared memory.
 template <int BITS, bool PAIRED>
 __device__ __forceinline__ void kstep_mma(const uint8_t* __restrict__ ch, const __half* __restrict__ bk, int bm_set,
-                                          int lane, float (&acc)[4], float (&acc2)[4]) {
-  kstep_compute<BITS, PAIRED>(kwords_smem<BITS>(ch, lane), bk, bm_set, lane, acc, acc2);
-}
-
-// A warp's partial outputs of one task for the reduction buffer: per
-// output, fma(acc, 2^24, accm) of its hi part plus that of its lo part.
-// Paired: columns (2q, 2q + 1) of a lane are row q's hi and lo parts, so
-// the lane's two outputs (weight rows g, g + 8) land in .x and .z; two-set:
-// the lane's four outputs (rows 2q, 2q + 1 at g, g + 8) in .x .y .z .w.
-template <bool PAIRED>
-__device__ __forceinline__ float4 partials(const float (&acc)[4], const float (&accm)[4], const float (&acc2)[4],
-                                           const float (&accm2)[4]) {
-  float h[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = fmaf(acc[i], kDqUnscale, accm[i]);
-  if constexpr (PAIRED) {
-    return make_float4(h[0] + h[1], 0.f, h[2] + h[3], 0.f);
-  } else {
-    float l[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) l[i] = fmaf(acc2[i], kDqUnscale, accm2[i]);
-    return make_float4(h[0] + l[0], h[1] + l[1], h[2] + l[2], h[3] + l[3]);
-  }
+                                          int lane, float (&acc)[4]) {
+  kstep_compute<BITS, PAIRED>(kwords_smem<BITS>(ch, lane), bk, bm_set, lane, acc);
 }
 
 // This warp's share of one staged chunk of its sub-tile: k-steps [k0, k1)
@@ -301,8 +290,8 @@ template <int BITS, bool PAIRED, bool VMAP = false>
 __device__ __forceinline__ void chunk_mma(const uint8_t* __restrict__ sub, int mins_off, int ks_base, int k0, int k1,
                                           int mk_base, int m0, int m1, const __half* __restrict__ bm,
                                           const __half* __restrict__ bs, int bm_set, int bs_set, int lane_b, int lane,
-                                          float (&acc)[4], float (&accm)[4], float (&acc2)[4], float (&accm2)[4],
-                                          int kph = 0, int kpg = 0) {
+                                          float (&acc)[4], float (&accm)[4], float (&accm2)[4], int kph = 0,
+                                          int kpg = 0) {
   constexpr int S = Fmt<BITS>::kBHalves;
   const uint8_t* a = sub + k0 * Fmt<BITS>::kChunk;
   const __half* bk = bm + (ks_base + k0) * 32 * S + lane_b * 8;
@@ -312,7 +301,7 @@ __device__ __forceinline__ void chunk_mma(const uint8_t* __restrict__ sub, int m
       const int ks = ks_base + kl;
       bk = bm + (((ks >> kpg) << kph) + (ks & ((1 << kph) - 1))) * 32 * S + lane_b * 8;
     }
-    kstep_mma<BITS, PAIRED>(a, bk, bm_set, lane, acc, acc2);
+    kstep_mma<BITS, PAIRED>(a, bk, bm_set, lane, acc);
     a += Fmt<BITS>::kChunk;
     bk += 32 * S;
   }
@@ -1430,8 +1419,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
     // the previous task's barrier guarantees no warp still reads the old activations
     if (tk.group != gs.cur) enter_group<BITS, PHASE>(L, W, C, sp, tk, K, rg.abort_flag, bm, bs, gs);
     const int kv = (PHASE == 1 && tk.shared) ? 1 : 0;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
-    float acc2[4] = {0.f, 0.f, 0.f, 0.f}, accm2[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f}, accm2[4] = {0.f, 0.f, 0.f, 0.f};
     if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 0);
     for (int ch = 0; ch < P.nchunks; ++ch) {
       const int ks0 = P.cks[kv][ch], ks1 = P.cks[kv][ch + 1];
@@ -1446,11 +1434,11 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
         constexpr bool kVmap = PHASE == 3;
         if (gs.paired)
           chunk_mma<BITS, true, kVmap>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
-                                       C.bsum_halves, gs.lane_b, lane, acc, accm, acc2, accm2, L.kph_log2,
+                                       C.bsum_halves, gs.lane_b, lane, acc, accm, accm2, L.kph_log2,
                                        L.kpg_log2);
         else
           chunk_mma<BITS, false, kVmap>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
-                                        C.bsum_halves, gs.lane_b, lane, acc, accm, acc2, accm2, L.kph_log2,
+                                        C.bsum_halves, gs.lane_b, lane, acc, accm, accm2, L.kph_log2,
                                         L.kpg_log2);
       }
       __syncwarp();
@@ -1459,7 +1447,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
     }
     if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 2);
     float4* rb = red + buf * (kConsumerWarps * 32);
-    rb[warp * 32 + lane] = gs.paired ? partials<true>(acc, accm, acc2, accm2) : partials<false>(acc, accm, acc2, accm2);
+    rb[warp * 32 + lane] = gs.paired ? partials<true>(acc, accm, accm2) : partials<false>(acc, accm, accm2);
     consumer_sync();  // all 16 warps: the ring path's warps stay in step
     if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 3);
 
@@ -1635,8 +1623,7 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
         enter_group<BITS, PHASE>(L, W, C, sp, tk, K, abort_flag, bm, bs, gs);
       }
       const ItemRange r = item_range<BITS, NS>(K, kg);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f};
-      float acc2[4] = {0.f, 0.f, 0.f, 0.f}, accm2[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f}, accm2[4] = {0.f, 0.f, 0.f, 0.f};
       const __half* bk = bm + r.k0 * 32 * S + gs.lane_b * 8;
       const __half* bsm = bs + r.m0 * 128 + gs.lane_b * 4;
       // refill the slot just used with the stream's next item, then move on
@@ -1653,7 +1640,7 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
         for (int ci = 0; ci < r.nk; ++ci) {
           cp_async_wait_group<kDepth - 1>();
           __syncwarp();
-          kstep_mma<BITS, true>(it, bk, C.bmain_halves, lane, acc, acc2);
+          kstep_mma<BITS, true>(it, bk, C.bmain_halves, lane, acc);
           bk += 32 * S;
           next_slot();
         }
@@ -1661,7 +1648,7 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
         for (int ci = 0; ci < r.nk; ++ci) {
           cp_async_wait_group<kDepth - 1>();
           __syncwarp();
-          kstep_mma<BITS, false>(it, bk, C.bmain_halves, lane, acc, acc2);
+          kstep_mma<BITS, false>(it, bk, C.bmain_halves, lane, acc);
           bk += 32 * S;
           next_slot();
         }
@@ -1680,8 +1667,7 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
         next_slot();
       }
       float4* rb = red + buf * (kConsumerWarps * 32);
-      rb[warp * 32 + lane] =
-          gs.paired ? partials<true>(acc, accm, acc2, accm2) : partials<false>(acc, accm, acc2, accm2);
+      rb[warp * 32 + lane] = gs.paired ? partials<true>(acc, accm, accm2) : partials<false>(acc, accm, accm2);
       og.sync();
       {
         constexpr int kGT = OutGroup<PHASE, NS>::kThreads;
