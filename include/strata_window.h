@@ -151,6 +151,24 @@ strata_status strata_window_create(const strata_moe_desc* desc, const strata_moe
  * (no plan fits the limit: create would fail the same way). */
 strata_status strata_window_plan(const strata_moe_desc* desc, int32_t smem_limit, strata_window_info* info);
 
+/* The slots of the next window when more slots are open than one window
+ * holds.  The Strata docs ("BATCHING.md", --batch-mtp paragraph): a window
+ * carries each active slot's rows (its token, and its MTP proposal with
+ * --batch-mtp), at most 8 rows, so at most four slots with proposals are in
+ * one window, and more slots rotate through.  The rule here (a reading):
+ * starting at slot `start`, slots are taken in cyclic order, each at most
+ * once, while their rows still fit in max_rows; a slot with no rows is
+ * skipped; the next window starts at the slot after the last one taken.  The
+ * window's rows are the taken slots' rows in this order, each slot's rows
+ * consecutive (token row, then proposal row), which is the layout
+ * strata_head_forward's proposal check reads.
+ *   rows_per_slot: host [n_slots], each 0..max_rows; slots_out: host
+ *   [n_slots] receives the window's slots, *n_out their number;
+ *   *next_start the next window's start.  Host only: no device is touched.
+ * Returns EINVAL for a bad argument. */
+strata_status strata_window_slots(int32_t n_slots, const int32_t* rows_per_slot, int32_t start, int32_t max_rows,
+                                  int32_t* slots_out, int32_t* n_out, int32_t* next_start);
+
 /* Run one window: y = MoE(x) for T rows.
  *   x: device fp32 [T][d], caller-owned; y: device fp32 [T][d], caller-owned,
  *   must not overlap x; both 16-byte aligned.  1 <= T <= desc.max_rows.

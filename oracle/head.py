@@ -114,3 +114,29 @@ def verify_slots(tokens: Sequence[int], fed: Sequence[int]) -> List[int]:
             t += 1
         n[start] = emit
     return n
+
+
+def window_slots(rows_per_slot: Sequence[int], start: int, max_rows: int = 8):
+    """Slots of the next window when more slots are open than one window holds.
+
+    The pages ("BATCHING.md", --batch-mtp paragraph): a window carries each
+    active slot's rows (its token, plus its proposal with --batch-mtp), at most
+    8 rows, and more slots rotate through.  Reading: starting at slot
+    ``start``, slots are taken in cyclic order, each once, while their rows
+    still fit; a slot with no rows is skipped; the next window starts at the
+    slot after the last one taken.  Returns (slots in window order, next start).
+    """
+    n = len(rows_per_slot)
+    taken, used = [], 0
+    last = start - 1
+    for i in range(n):
+        s = (start + i) % n
+        r = int(rows_per_slot[s])
+        if r <= 0:
+            continue
+        if used + r > max_rows:
+            break
+        taken.append(s)
+        used += r
+        last = s
+    return taken, (last + 1) % n if n else 0

@@ -26,7 +26,8 @@ EXPORTED = ("strata_window_create", "strata_moe_window_forward", "strata_window_
             "strata_stack_query", "strata_stack_set_profiling", "strata_stack_timings", "strata_stack_destroy",
             "strata_window_plan", "strata_tier_create", "strata_window_set_tier", "strata_tier_read",
             "strata_tier_destroy", "strata_head_create", "strata_head_forward", "strata_head_sync",
-            "strata_head_query", "strata_head_set_profiling", "strata_head_timings", "strata_head_destroy")
+            "strata_head_query", "strata_head_set_profiling", "strata_head_timings", "strata_head_destroy",
+            "strata_window_slots")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -180,6 +181,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.strata_head_timings.restype = ctypes.c_int
     lib.strata_head_destroy.argtypes = [ctypes.c_void_p]
     lib.strata_head_destroy.restype = ctypes.c_int
+    lib.strata_window_slots.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_void_p, P(ctypes.c_int32), P(ctypes.c_int32)]
+    lib.strata_window_slots.restype = ctypes.c_int
     lib.strata_status_str.argtypes = [ctypes.c_int]
     lib.strata_status_str.restype = ctypes.c_char_p
     _lib = lib
@@ -356,6 +360,16 @@ def strata_head_timings(handle):
 
 def strata_head_destroy(handle) -> int:
     return load().strata_head_destroy(ctypes.c_void_p(handle) if handle else None)
+
+
+def strata_window_slots(rows_per_slot, start: int, max_rows: int = 8):
+    """Returns (status, slots of the next window, next start)."""
+    n = len(rows_per_slot)
+    rows = (ctypes.c_int32 * max(n, 1))(*[int(r) for r in rows_per_slot])
+    out = (ctypes.c_int32 * max(n, 1))()
+    cnt, nxt = ctypes.c_int32(), ctypes.c_int32()
+    st = load().strata_window_slots(n, rows if n else None, start, max_rows, out, ctypes.byref(cnt), ctypes.byref(nxt))
+    return st, [out[i] for i in range(cnt.value)] if st == STRATA_OK else [], nxt.value
 
 
 def check(status: int, what: str) -> None:

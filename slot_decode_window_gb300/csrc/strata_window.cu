@@ -98,6 +98,27 @@ const char* strata_status_str(strata_status s) {
 constexpr int kStaticSmemReserve = 12288;
 constexpr int kGb300SmemOptin = 232448;
 
+strata_status strata_window_slots(int32_t n_slots, const int32_t* rows_per_slot, int32_t start, int32_t max_rows,
+                                  int32_t* slots_out, int32_t* n_out, int32_t* next_start) {
+  if (n_slots < 1 || !rows_per_slot || !slots_out || !n_out || !next_start) return STRATA_EINVAL;
+  if (start < 0 || start >= n_slots || max_rows < 1 || max_rows > kMaxRows) return STRATA_EINVAL;
+  for (int s = 0; s < n_slots; ++s)
+    if (rows_per_slot[s] < 0 || rows_per_slot[s] > max_rows) return STRATA_EINVAL;
+  int n = 0, used = 0, last = start - 1;
+  for (int i = 0; i < n_slots; ++i) {
+    const int s = (start + i) % n_slots;
+    const int r = rows_per_slot[s];
+    if (r == 0) continue;
+    if (used + r > max_rows) break;
+    slots_out[n++] = s;
+    used += r;
+    last = s;
+  }
+  *n_out = n;
+  *next_start = ((last + 1) % n_slots + n_slots) % n_slots;
+  return STRATA_OK;
+}
+
 strata_status strata_window_plan(const strata_moe_desc* desc, int32_t smem_limit, strata_window_info* info) {
   if (!info) return STRATA_EINVAL;
   std::memset(info, 0, sizeof(*info));
