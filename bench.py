@@ -763,6 +763,37 @@ def measure_stack(args, dev, flush, stream, peak, cpu_jobs=None):
            "rows_per_s": steps * T / tot, "algorithmic_bytes_per_window": nbytes / steps,
            "achieved_GBps": achieved, "peak_GBps": peak, "frac": achieved / peak,
            "kernel": "stack_kernel<4> (one cooperative launch per window)", "gpu_launches_per_window": 1}
+
+    # the same stack attending over each slot's KV cache: 4 slots x (token,
+    # proposal) at positions 1000 and 1001 over 1000 positions of history
+    n_slots, max_ctx, hist = 4, 1024, 1000
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    shape = (wl.n_layers, n_slots, wl.kv_heads, max_ctx, wl.head_dim)
+    kc = torch.randn(shape, generator=g, device=dev).to(torch.float16)
+    vc = torch.randn(shape, generator=g, device=dev).to(torch.float16)
+    stk.set_kv(kc, vc, n_slots, max_ctx)
+    slot = torch.tensor([0, 0, 1, 1, 2, 2, 3, 3], dtype=torch.int32, device=dev)
+    pos = torch.tensor([hist, hist + 1] * 4, dtype=torch.int32, device=dev)
+    kv_bytes = wl.n_layers * n_slots * 2 * wl.kv_heads * (hist + 2) * wl.head_dim * 2
+    for i in range(warm):
+        stk.forward(X[i % nw], Y, slot=slot, position=pos)
+    stk.set_profiling(True)
+    ms2, nb2 = [], 0.0
+    for i in range(steps):
+        flush_and_hold(flush)
+        stk.forward(X[i % nw], Y, slot=slot, position=pos)
+        ms2.append(stk.timings())
+        nb2 += per_window[i % nw] + kv_bytes
+    stk.set_profiling(False)
+    stk.sync()
+    tot2 = sum(ms2) / 1e3
+    out["with_kv_cache"] = {
+        "workload": "the same 48 layers attending over fp16 KV caches: 4 slots x (token, proposal) rows at "
+                    "positions 1000 and 1001, 1000 positions of history per slot",
+        "ms_per_window_median": statistics.median(ms2), "rows_per_s": steps * T / tot2,
+        "kv_bytes_per_window": kv_bytes, "algorithmic_bytes_per_window": nb2 / steps,
+        "achieved_GBps": nb2 / tot2 / 1e9, "frac": nb2 / tot2 / 1e9 / peak}
     stk.close()
     return out
 

@@ -270,6 +270,46 @@ strata_status strata_stack_create(int32_t n_layers, const strata_moe_desc* moe, 
 strata_status strata_stack_forward(strata_stack* s, const float* x, int32_t T, float* y, const strata_stack_out* out,
                                    void* cuda_stream);
 
+/* Attention over each slot's KV cache instead of the length-one reading.
+ *
+ * The Strata docs ("BATCHING.md", "Several requests at once (batch slots)")
+ * keep one KV cache per conversation slot; a verify window carries one row per
+ * slot, plus the slot's MTP proposal as a second row at the next position.
+ * With a cache set, each layer of strata_stack_forward_kv does, after the
+ * q/k/v projections: every row t (slot s_t, position p_t) stores its k and v,
+ * rounded to fp16, at position p_t of its slot in that layer's cache; then
+ * row t attends, for query head h, over positions 0..p_t of its slot with kv
+ * head h / (heads / kv_heads): softmax_j(q_h . K_j / sqrt(head_dim)) applied
+ * to the V_j (fp32 arithmetic; no position encoding, the pages name none).
+ * A proposal row at p + 1 thus sees its token row's entry at p written in the
+ * same window.  The o projection then reads this output in place of the
+ * length-one broadcast of v.
+ *   k, v: device fp16 bit patterns [n_layers][n_slots][kv_heads][max_ctx]
+ *   [head_dim], caller-owned and 16-byte aligned; positions below a row's are
+ *   the conversation's history, which the caller writes; the window writes
+ *   its rows' entries.  The caches must outlive their use.
+ * Requires head_dim a multiple of 32 and at most 128 (EUNSUPPORTED
+ * otherwise).  The stack allocates its attention scratch here (ENOMEM).  NULL
+ * drops the caches and frees that scratch. */
+typedef struct {
+  uint16_t* k;
+  uint16_t* v;
+  int32_t n_slots;
+  int32_t max_ctx;
+} strata_kv_cache;
+
+strata_status strata_stack_set_kv(strata_stack* s, const strata_kv_cache* kv);
+
+/* A window through every layer with attention over the caches set by
+ * strata_stack_set_kv (EINVAL when none is set): slot and position are
+ * device int32 [T].  Rows must have distinct (slot, position) pairs.  A row
+ * whose slot or position is out of range is left out of the caches, attends
+ * to nothing (zero attention output) and makes the next strata_stack_sync
+ * report EDEVICE.  Otherwise as strata_stack_forward (which always uses the
+ * length-one reading). */
+strata_status strata_stack_forward_kv(strata_stack* s, const float* x, int32_t T, float* y, const int32_t* slot,
+                                      const int32_t* position, const strata_stack_out* out, void* cuda_stream);
+
 /* Wait for the last stack_forward; EDEVICE if the GPU recorded an error. */
 strata_status strata_stack_sync(strata_stack* s);
 

@@ -27,7 +27,7 @@ EXPORTED = ("strata_window_create", "strata_moe_window_forward", "strata_window_
             "strata_window_plan", "strata_tier_create", "strata_window_set_tier", "strata_tier_read",
             "strata_tier_destroy", "strata_head_create", "strata_head_forward", "strata_head_sync",
             "strata_head_query", "strata_head_set_profiling", "strata_head_timings", "strata_head_destroy",
-            "strata_window_slots")
+            "strata_window_slots", "strata_stack_set_kv", "strata_stack_forward_kv")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -89,6 +89,11 @@ class strata_tier_desc(ctypes.Structure):
 
 class strata_tier_stats(ctypes.Structure):
     _fields_ = [("windows", ctypes.c_int64), ("rounds", ctypes.c_int64), ("n_swaps", ctypes.c_int32)]
+
+
+class strata_kv_cache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("n_slots", ctypes.c_int32),
+                ("max_ctx", ctypes.c_int32)]
 
 
 class strata_head_desc(ctypes.Structure):
@@ -184,6 +189,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.strata_window_slots.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_void_p, P(ctypes.c_int32), P(ctypes.c_int32)]
     lib.strata_window_slots.restype = ctypes.c_int
+    lib.strata_stack_set_kv.argtypes = [ctypes.c_void_p, P(strata_kv_cache)]
+    lib.strata_stack_set_kv.restype = ctypes.c_int
+    lib.strata_stack_forward_kv.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_void_p, P(strata_stack_out), ctypes.c_void_p]
+    lib.strata_stack_forward_kv.restype = ctypes.c_int
     lib.strata_status_str.argtypes = [ctypes.c_int]
     lib.strata_status_str.restype = ctypes.c_char_p
     _lib = lib
@@ -372,6 +382,17 @@ def strata_window_slots(rows_per_slot, start: int, max_rows: int = 8):
     return st, [out[i] for i in range(cnt.value)] if st == STRATA_OK else [], nxt.value
 
 
+def strata_stack_set_kv(handle, kv) -> int:
+    return load().strata_stack_set_kv(ctypes.c_void_p(handle), ctypes.byref(kv) if kv is not None else None)
+
+
+def strata_stack_forward_kv(handle, x_ptr: int, T: int, y_ptr: int, slot_ptr: int, pos_ptr: int,
+                            out: Optional["strata_stack_out"] = None, stream: int = 0) -> int:
+    return load().strata_stack_forward_kv(ctypes.c_void_p(handle), ctypes.c_void_p(x_ptr), T, ctypes.c_void_p(y_ptr),
+                                          ctypes.c_void_p(slot_ptr), ctypes.c_void_p(pos_ptr),
+                                          ctypes.byref(out) if out is not None else None, ctypes.c_void_p(stream))
+
+
 def check(status: int, what: str) -> None:
     if status != STRATA_OK:
         raise StrataError(status, what)
@@ -508,8 +529,21 @@ class Stack:
         check(st, "strata_stack_query")
         return info
 
-    def forward(self, x, y=None, outputs: bool = False, stream=None):
-        """Enqueue one window on x [T][d]; returns y (and per-layer q, k, routing)."""
+    def set_kv(self, k, v, n_slots: int, max_ctx: int) -> None:
+        """Attend over the fp16 caches k, v (CUDA tensors of
+        [n_layers][n_slots][kv_heads][max_ctx][head_dim], float16) from now on
+        (forward with slot and position); None drops them."""
+        if k is None:
+            check(strata_stack_set_kv(self.handle, None), "strata_stack_set_kv")
+            self.kv = None
+            return
+        check(strata_stack_set_kv(self.handle, strata_kv_cache(k.data_ptr(), v.data_ptr(), n_slots, max_ctx)),
+              "strata_stack_set_kv")
+        self.kv = (k, v)
+
+    def forward(self, x, y=None, outputs: bool = False, stream=None, slot=None, position=None):
+        """Enqueue one window on x [T][d]; returns y (and per-layer q, k, routing).
+        With slot and position (CUDA int32 [T]) the window attends over the caches set by set_kv."""
         import torch
         assert x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()
         T, d = x.shape
@@ -527,7 +561,11 @@ class Stack:
                        n_distinct=torch.empty(n, dtype=torch.int32, device=dev))
             o = strata_stack_out(*(res[m].data_ptr() for m in ("q", "k", "topk_idx", "topk_w", "n_distinct")))
         s = (stream or torch.cuda.current_stream()).cuda_stream
-        check(strata_stack_forward(self.handle, x.data_ptr(), T, y.data_ptr(), o, s), "strata_stack_forward")
+        if slot is not None:
+            check(strata_stack_forward_kv(self.handle, x.data_ptr(), T, y.data_ptr(), slot.data_ptr(),
+                                          position.data_ptr(), o, s), "strata_stack_forward_kv")
+        else:
+            check(strata_stack_forward(self.handle, x.data_ptr(), T, y.data_ptr(), o, s), "strata_stack_forward")
         return (y, res) if outputs else y
 
     def set_profiling(self, enable: bool) -> None:

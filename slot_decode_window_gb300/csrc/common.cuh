@@ -104,6 +104,25 @@ struct TierDev {
   float decay, min_gain;
 };
 
+// A stack window's attention over each slot's KV cache (stack kernel only; a
+// null k means the length-one reading: every query head outputs v of its kv
+// head).  The caches are the caller's; the rest is the stack's scratch.
+struct KVDev {
+  __half* k;               // [n_layers][n_slots][kv_heads][max_ctx][head_dim] fp16
+  __half* v;               // the same for values
+  int n_slots, max_ctx, head_dim;
+  int nch;                 // chunks of kAttnChunk positions in max_ctx (rounded up)
+  const int* slot;         // [T] each row's slot
+  const int* pos;          // [T] each row's position
+  float* qbuf;             // [kMaxRows][dq] the rows' q
+  float* kbuf;             // [kMaxRows][dkv] the rows' k
+  float* part;             // [kMaxRows][heads][nch][head_dim + 2] per-chunk partials (o, max, sum)
+  __half* afrag;           // the o projection's B operand (att), in the shared-memory B layout, 2 sets
+  int afrag_set;           // halves per set of afrag (8 x dq)
+  float* asum;             // [kMaxRows][dq / block] block sums of att
+};
+constexpr int kAttnChunk = 64;  // cache positions per attention work item
+
 struct WindowBufs {
   const float* x;          // [T][d]
   float* y;                // [T][d]
@@ -130,6 +149,7 @@ struct WindowBufs {
   int njb;                 // column chunks of the router GEMV
   unsigned* err;
   TierDev tier;            // adaptive tier bookkeeping (single-layer windows; counters null = none)
+  KVDev kv;                // attention over KV caches (stack kernel; k null = the length-one reading)
   long long wait_cycles;   // limit of every bounded device wait, in SM clock cycles
   int bar_extra;           // arrivals a grid barrier expects beyond the grid (0; > 0 only in failure tests)
   // decoder-layer extras (stack kernel only; null in the single-layer kernel)

@@ -27,6 +27,7 @@ struct strata_stack {
   bool profiling = false;
   bool profiled_once = false;
   cudaEvent_t prof[2] = {nullptr, nullptr};
+  void* kvmem = nullptr;             // the cache attention's scratch (strata_stack_set_kv)
 };
 
 namespace {
@@ -62,6 +63,7 @@ void free_stack(strata_stack* s) {
   if (s->dense) cudaFree(s->dense);
   if (s->dev_layers) cudaFree(s->dev_layers);
   if (s->extra) cudaFree(s->extra);
+  if (s->kvmem) cudaFree(s->kvmem);
   if (s->done) cudaEventDestroy(s->done);
   for (cudaEvent_t& ev : s->prof)
     if (ev) cudaEventDestroy(ev);
@@ -193,8 +195,68 @@ strata_status strata_stack_create(int32_t n_layers, const strata_moe_desc* moe, 
   return STRATA_OK;
 }
 
-strata_status strata_stack_forward(strata_stack* s, const float* x, int32_t T, float* y, const strata_stack_out* out,
-                                   void* cuda_stream) {
+strata_status strata_stack_set_kv(strata_stack* s, const strata_kv_cache* kv) {
+  if (!s) return STRATA_EINVAL;
+  if (!kv) {
+    if (s->kvmem) cudaFree(s->kvmem);
+    s->kvmem = nullptr;
+    s->W.kv = KVDev{};
+    return STRATA_OK;
+  }
+  const int hd = s->attn.head_dim, H = s->attn.heads, kvh = s->attn.kv_heads, grp = H / kvh;
+  if (!kv->k || !kv->v || kv->n_slots < 1 || kv->max_ctx < 1 || kv->max_ctx > (1 << 20)) return STRATA_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(kv->k) | reinterpret_cast<uintptr_t>(kv->v)) % 16 != 0) return STRATA_EINVAL;
+  // the attention phase takes 32 to 128 head dimensions (whole lanes of a
+  // warp) and keeps one chunk of keys and values, the rows' queries and their
+  // scores in the shared-memory ring
+  const long long need = 2LL * kAttnChunk * hd * 2 + (long long)kMaxRows * grp * hd * 4 +
+                         (long long)kMaxRows * grp * kAttnChunk * 4;
+  if (hd % 32 != 0 || hd > 128 || need > (long long)s->cfg.nstages * s->cfg.stage_bytes) return STRATA_EUNSUPPORTED;
+  const int dq = H * hd, dkv = kvh * hd, block = s->desc.block;
+  const int nch = (kv->max_ctx + kAttnChunk - 1) / kAttnChunk;
+  size_t w = 0;
+  const size_t o_q = w; w = align_up(w + (size_t)kMaxRows * dq * 4, 256);
+  const size_t o_k = w; w = align_up(w + (size_t)kMaxRows * dkv * 4, 256);
+  const size_t o_p = w; w = align_up(w + (size_t)kMaxRows * H * nch * (hd + 2) * 4, 256);
+  const size_t o_a = w; w = align_up(w + (size_t)2 * 8 * dq * 2, 256);
+  const size_t o_s = w; w = align_up(w + (size_t)kMaxRows * (dq / block) * 4, 256);
+  void* mem = nullptr;
+  if (cudaMalloc(&mem, w) != cudaSuccess) {
+    cudaGetLastError();
+    return STRATA_ENOMEM;
+  }
+  if (cudaMemset(mem, 0, w) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(mem);
+    return STRATA_ECUDA;
+  }
+  if (s->kvmem) cudaFree(s->kvmem);
+  s->kvmem = mem;
+  uint8_t* b = static_cast<uint8_t*>(mem);
+  KVDev& K = s->W.kv;
+  K.k = reinterpret_cast<__half*>(kv->k);
+  K.v = reinterpret_cast<__half*>(kv->v);
+  K.n_slots = kv->n_slots;
+  K.max_ctx = kv->max_ctx;
+  K.head_dim = hd;
+  K.nch = nch;
+  K.slot = nullptr;
+  K.pos = nullptr;
+  K.qbuf = reinterpret_cast<float*>(b + o_q);
+  K.kbuf = reinterpret_cast<float*>(b + o_k);
+  K.part = reinterpret_cast<float*>(b + o_p);
+  K.afrag = reinterpret_cast<__half*>(b + o_a);
+  K.afrag_set = 8 * dq;
+  K.asum = reinterpret_cast<float*>(b + o_s);
+  return STRATA_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+strata_status stack_launch(strata_stack* s, const float* x, int32_t T, float* y, const strata_stack_out* out,
+                           const int32_t* slot, const int32_t* position, void* cuda_stream) {
   if (!s || !x || !y) return STRATA_EINVAL;
   if (T < 1 || T > s->desc.max_rows) return STRATA_EINVAL;
   const size_t bytes = (size_t)T * s->desc.hidden * sizeof(float);
@@ -204,6 +266,12 @@ strata_status strata_stack_forward(strata_stack* s, const float* x, int32_t T, f
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) % 16 != 0) return STRATA_EINVAL;
   cudaStream_t cs = static_cast<cudaStream_t>(cuda_stream);
   WindowBufs W = s->W;
+  if (slot) {
+    W.kv.slot = slot;
+    W.kv.pos = position;
+  } else {
+    W.kv = KVDev{};  // the length-one reading
+  }
   W.x = x;
   W.y = y;
   W.T = T;
@@ -225,6 +293,21 @@ strata_status strata_stack_forward(strata_stack* s, const float* x, int32_t T, f
     return STRATA_ECUDA;
   }
   return STRATA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+strata_status strata_stack_forward(strata_stack* s, const float* x, int32_t T, float* y, const strata_stack_out* out,
+                                   void* cuda_stream) {
+  return stack_launch(s, x, T, y, out, nullptr, nullptr, cuda_stream);
+}
+
+strata_status strata_stack_forward_kv(strata_stack* s, const float* x, int32_t T, float* y, const int32_t* slot,
+                                      const int32_t* position, const strata_stack_out* out, void* cuda_stream) {
+  if (!s || !slot || !position || !s->W.kv.k) return STRATA_EINVAL;
+  return stack_launch(s, x, T, y, out, slot, position, cuda_stream);
 }
 
 strata_status strata_stack_sync(strata_stack* s) {

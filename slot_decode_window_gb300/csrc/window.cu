@@ -1022,6 +1022,27 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
       }
     }
     cp_async_wait_all();
+  } else if (W.kv.k) {
+    // the o projection's input is the cache attention's output: its main
+    // fragments stay in global memory (kv_combine wrote them in this layout);
+    // its block sums are split into hi/lo here
+    const int nb = L.dq / B;
+    zero_padded_sums(bs, C, nb, (nb + 15) / 16, R, paired, ctid);
+    for (int i = ctid; i < R * nb; i += kConsumerThreads) {
+      const int r = i / nb, blk = i - r * nb;
+      __half hi, lo;
+      split_hi_lo(__ldcg(W.kv.asum + (long long)r * nb + blk), hi, lo);
+      const int spos = frag_sum_pos(blk);
+      const int mk = spos >> 4, c = (spos >> 2) & 3, slot = spos & 3;
+      const int o = mk * 128 + c * 4 + slot;
+      if (paired) {
+        bs[o + (2 * r) * 16] = hi;
+        bs[o + (2 * r + 1) * 16] = lo;
+      } else {
+        bs[o + r * 16] = hi;
+        bs[C.bsum_halves + o + r * 16] = lo;
+      }
+    }
   } else {
     zero_padded_sums(bs, C, L.dq / B, (L.dq / B + 15) / 16, R, paired, ctid);
     // v (K = dkv): one element per thread and step; a warp covers 32
@@ -1380,11 +1401,13 @@ __device__ __forceinline__ void task_epilogue(const LayerDev& L, const WindowBuf
       for (int w = 0; w < kWPS; ++w) v += frag_pick(rb[(s * kWPS + w) * 32 + src_lane], idx, gs.paired);
       const int drow = (tk.tile + s) * 16 + row;
       if constexpr (PHASE == 2) {
-        // rows of [Wq; Wk; Wv]
+        // rows of [Wq; Wk; Wv] (q and k also kept for the cache attention)
         if (drow < L.dq) {
           if (W.q_out) W.q_out[(long long)r * L.dq + drow] = v;
+          if (W.kv.qbuf) W.kv.qbuf[(long long)r * L.dq + drow] = v;
         } else if (drow < L.dq + L.dkv) {
           if (W.k_out) W.k_out[(long long)r * L.dkv + drow - L.dq] = v;
+          if (W.kv.kbuf) W.kv.kbuf[(long long)r * L.dkv + drow - L.dq] = v;
         } else {
           W.v[(long long)r * L.dkv + drow - L.dq - L.dkv] = v;
         }
@@ -1431,15 +1454,27 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
       if (wait_bar(&rg.full[stage], rp.parity, W.err, rg.abort_flag, W.wait_cycles)) {
         if (PHASE < 2 && ch == 0) TRACE(0, PHASE, task - pt.t0, 1);
         const uint8_t* st = rg.base + (size_t)stage * C.stage_bytes + sub * P.sub_stride;
-        constexpr bool kVmap = PHASE == 3;
-        if (gs.paired)
-          chunk_mma<BITS, true, kVmap>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
-                                       C.bsum_halves, gs.lane_b, lane, acc, accm, accm2, L.kph_log2,
-                                       L.kpg_log2);
-        else
-          chunk_mma<BITS, false, kVmap>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
+        if (PHASE == 3 && !W.kv.k) {  // the length-one reading: v's fragments, k-steps remapped
+          if (gs.paired)
+            chunk_mma<BITS, true, true>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
                                         C.bsum_halves, gs.lane_b, lane, acc, accm, accm2, L.kph_log2,
                                         L.kpg_log2);
+          else
+            chunk_mma<BITS, false, true>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bm, bs, C.bmain_halves,
+                                         C.bsum_halves, gs.lane_b, lane, acc, accm, accm2, L.kph_log2,
+                                         L.kpg_log2);
+        } else {
+          // (phase 3 with the cache attention: B is the attention output's
+          // fragments in global memory, kv.afrag)
+          const __half* bmx = PHASE == 3 ? W.kv.afrag : bm;
+          const int bset = PHASE == 3 ? W.kv.afrag_set : C.bmain_halves;
+          if (gs.paired)
+            chunk_mma<BITS, true, false>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bmx, bs, bset, C.bsum_halves,
+                                         gs.lane_b, lane, acc, accm, accm2);
+          else
+            chunk_mma<BITS, false, false>(st, P.mins_off, ks0, k0, k1, mk0, m0, m1, bmx, bs, bset, C.bsum_halves,
+                                          gs.lane_b, lane, acc, accm, accm2);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&rg.empty[stage]);
@@ -2038,6 +2073,231 @@ __global__ void __launch_bounds__(kConsumerThreads, 1) window_kernel_direct(Laye
   }
 }
 
+// ---------------------------------------------------------------------------
+// attention over each slot's KV cache (stack kernel)
+// ---------------------------------------------------------------------------
+// The Strata docs ("BATCHING.md", "Several requests at once (batch slots)")
+// keep one KV cache per slot; a verify window carries one row per slot, plus
+// the slot's MTP proposal as a second row at the next position.  Here a row t
+// of slot s_t at position p_t stores its k and v (fp16) at p_t, and then
+// attends, for query head h, over positions 0..p_t of its slot with kv head
+// h / (heads / kv_heads): softmax_j(q_h . K_j / sqrt(head_dim)) applied to the
+// V_j.  No position encoding (the pages name none).
+
+__device__ __forceinline__ bool kv_row_ok(const KVDev& K, int t) {
+  const int s = K.slot[t], p = K.pos[t];
+  return s >= 0 && s < K.n_slots && p >= 0 && p < K.max_ctx;
+}
+
+__device__ __forceinline__ long long kv_base(const KVDev& K, int layer, int kvh, int slot, int g) {
+  return (((long long)layer * K.n_slots + slot) * kvh + g) * K.max_ctx * K.head_dim;
+}
+
+// A0 (all CTAs): every row's k and v to position p_t of slot s_t, in fp16.
+// A row whose slot or position is out of range is flagged and left out.
+__device__ __noinline__ void kv_append(const LayerDev& L, const WindowBufs& W, int layer) {
+  const KVDev& K = W.kv;
+  const int hd = K.head_dim, kvh = L.dkv / hd;
+  const int n = W.T * L.dkv;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int t = i / L.dkv, f = i - t * L.dkv, g = f / hd, e = f - g * hd;
+    if (!kv_row_ok(K, t)) {
+      if (f == 0) atomicOr(W.err, kErrIndex);
+      continue;
+    }
+    const long long o = kv_base(K, layer, kvh, K.slot[t], g) + (long long)K.pos[t] * hd + e;
+    K.k[o] = __float2half_rn(K.kbuf[(long long)t * L.dkv + f]);
+    K.v[o] = __float2half_rn(W.v[(long long)t * L.dkv + f]);
+  }
+}
+
+// The window's valid rows grouped by slot, in first-row order: each group's
+// slot, row mask and largest position (every CTA computes the same).
+struct SlotGroups {
+  int n;
+  int slot[kMaxRows];
+  unsigned rows[kMaxRows];
+  int pmax[kMaxRows];
+};
+
+__device__ void group_slots(const WindowBufs& W, SlotGroups& G) {
+  const KVDev& K = W.kv;
+  G.n = 0;
+  for (int t = 0; t < W.T; ++t) {
+    if (!kv_row_ok(K, t)) continue;
+    const int s = K.slot[t], p = K.pos[t];
+    int i = 0;
+    while (i < G.n && G.slot[i] != s) ++i;
+    if (i == G.n) {
+      G.slot[i] = s;
+      G.rows[i] = 0u;
+      G.pmax[i] = p;
+      ++G.n;
+    }
+    G.rows[i] |= 1u << t;
+    G.pmax[i] = max(G.pmax[i], p);
+  }
+}
+
+// A1: per-chunk partials.  An item is (slot group, kv head g, chunk c of
+// kAttnChunk positions up to the group's largest position); it serves every
+// row of the group, so the two rows of a slot read its cache once.  For each
+// row r and query head h of kv head g: m = the largest score over the chunk's
+// positions j <= p_r, l = sum exp(s_j - m), o = sum exp(s_j - m) V_j (fp32,
+// fixed orders), written to kv.part.  Items are dealt out over the CTAs.
+// smem: K and V chunk (fp16), the rows' q, the scores / weights.
+__device__ __noinline__ void kv_partials(const LayerDev& L, const WindowBufs& W, int layer, uint8_t* smem) {
+  const KVDev& K = W.kv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+  const int hd = K.head_dim, kvh = L.dkv / hd, H = L.dq / hd, grp = H / kvh, dpl = hd / 32;
+  constexpr int C = kAttnChunk;
+  __shared__ SlotGroups G;
+  __shared__ int s_rows[kMaxRows];
+  if (tid == 0) group_slots(W, G);
+  __syncthreads();
+  __half* Ks = reinterpret_cast<__half*>(smem);
+  __half* Vs = Ks + C * hd;
+  float* qs = reinterpret_cast<float*>(Vs + C * hd);
+  float* sc = qs + kMaxRows * grp * hd;
+  const float scale = 1.0f / sqrtf((float)hd);
+  int n_items = 0;
+  for (int i = 0; i < G.n; ++i) n_items += kvh * ((G.pmax[i] + C) / C);
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    int i = 0, rem = item;
+    while (rem >= kvh * ((G.pmax[i] + C) / C)) {
+      rem -= kvh * ((G.pmax[i] + C) / C);
+      ++i;
+    }
+    const int nch_i = (G.pmax[i] + C) / C;
+    const int g = rem / nch_i, c = rem - g * nch_i;
+    const int j0 = c * C, n = min(C, G.pmax[i] + 1 - j0);
+    const unsigned rows = G.rows[i];
+    const int R = __popc(rows);
+    if (tid == 0) {
+      int r = 0;
+      for (int t = 0; t < W.T; ++t)
+        if (rows & (1u << t)) s_rows[r++] = t;
+    }
+    // K and V of positions j0 .. j0 + n - 1 (contiguous for one slot and head)
+    const long long base = kv_base(K, layer, kvh, G.slot[i], g) + (long long)j0 * hd;
+    const int pieces = n * hd / 8;
+    for (int q = tid; q < 2 * pieces; q += blockDim.x) {
+      const bool isv = q >= pieces;
+      const int qq = isv ? q - pieces : q;
+      cp_async16((isv ? Vs : Ks) + qq * 8, (isv ? K.v : K.k) + base + qq * 8);
+    }
+    __syncthreads();  // s_rows
+    for (int q = tid; q < R * grp * hd; q += blockDim.x) {
+      const int pr = q / hd, e = q - pr * hd, r = pr / grp, hh = pr - r * grp;
+      qs[q] = __ldcg(K.qbuf + (long long)s_rows[r] * L.dq + (g * grp + hh) * hd + e);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    // scores: warp per position, lanes over the head dimension
+    for (int j = warp; j < n; j += nw) {
+      float kk[4];
+#pragma unroll
+      for (int d = 0; d < 4; ++d) kk[d] = d < dpl ? __half2float(Ks[j * hd + lane * dpl + d]) : 0.f;
+      for (int pr = 0; pr < R * grp; ++pr) {
+        const float* qp = qs + pr * hd + lane * dpl;
+        float v = 0.f;
+#pragma unroll
+        for (int d = 0; d < 4; ++d)
+          if (d < dpl) v = fmaf(qp[d], kk[d], v);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) sc[pr * C + j] = v * scale;
+      }
+    }
+    __syncthreads();
+    // softmax statistics per (row, head) over the positions the row sees
+    for (int pr = warp; pr < R * grp; pr += nw) {
+      const int r = pr / grp, hh = pr - r * grp, t = s_rows[r];
+      const int jmax = K.pos[t] - j0;  // positions j <= jmax are the row's
+      float m = -INFINITY;
+      for (int j = lane; j < n; j += 32)
+        if (j <= jmax) m = fmaxf(m, sc[pr * C + j]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float l = 0.f;
+      for (int j = lane; j < n; j += 32) {
+        const float w = (j <= jmax && m != -INFINITY) ? expf(sc[pr * C + j] - m) : 0.f;
+        sc[pr * C + j] = w;
+        l += w;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+      if (lane == 0) {
+        float* pp = K.part + (((long long)t * H + g * grp + hh) * K.nch + c) * (hd + 2);
+        pp[hd] = m;
+        pp[hd + 1] = l;
+      }
+    }
+    __syncthreads();
+    // o = sum_j w_j V_j
+    for (int q = tid; q < R * grp * hd; q += blockDim.x) {
+      const int pr = q / hd, e = q - pr * hd, r = pr / grp, hh = pr - r * grp;
+      float o = 0.f;
+      for (int j = 0; j < n; ++j) o = fmaf(sc[pr * C + j], __half2float(Vs[j * hd + e]), o);
+      K.part[(((long long)s_rows[r] * H + g * grp + hh) * K.nch + c) * (hd + 2) + e] = o;
+    }
+    __syncthreads();  // the chunk buffers are reused by the next item
+  }
+}
+
+// A2: each row's attention output from its chunks' partials, written as the
+// o projection's B operand (fp16 hi/lo fragments in the shared-memory B
+// layout, kv.afrag) and per-block sums (kv.asum).  (row, head) pairs are dealt
+// out over the CTAs; thread e < head_dim takes element e of the head.
+template <int BITS>
+__device__ __noinline__ void kv_combine(const LayerDev& L, const WindowBufs& W) {
+  const KVDev& K = W.kv;
+  constexpr int S = Fmt<BITS>::kBHalves, B = Fmt<BITS>::kBlock;
+  const int tid = threadIdx.x, T = W.T, hd = K.head_dim, H = L.dq / hd;
+  constexpr int C = kAttnChunk;
+  const bool paired = T <= 4;
+  for (int q = blockIdx.x; q < T * H; q += gridDim.x) {
+    const int t = q / H, h = q - t * H;
+    if (tid >= hd) continue;
+    const int e = tid, f = h * hd + e;
+    float a = 0.f;
+    if (kv_row_ok(K, t)) {
+      const int nc = (K.pos[t] + C) / C;
+      const float* pp = K.part + ((long long)t * H + h) * K.nch * (hd + 2);
+      float M = -INFINITY;
+      for (int c = 0; c < nc; ++c) M = fmaxf(M, __ldcg(pp + c * (hd + 2) + hd));
+      float lsum = 0.f, o = 0.f;
+      for (int c = 0; c < nc; ++c) {
+        const float mc = __ldcg(pp + c * (hd + 2) + hd);
+        if (mc == -INFINITY) continue;
+        const float w = expf(mc - M);
+        lsum = fmaf(w, __ldcg(pp + c * (hd + 2) + hd + 1), lsum);
+        o = fmaf(w, __ldcg(pp + c * (hd + 2) + e), o);
+      }
+      a = lsum > 0.f ? o / lsum : 0.f;
+    }
+    int off;
+    float fac;
+    frag_main_pos<BITS>(f, off, fac);
+    const int ks = off / (4 * S), cq = (off / S) & 3, slot = off % S;
+    __half hi, lo;
+    split_hi_lo(a * fac, hi, lo);
+    if (paired) {
+      K.afrag[bmain_off<BITS>(ks, slot >> 3, 2 * t, cq) + (slot & 7)] = hi;
+      K.afrag[bmain_off<BITS>(ks, slot >> 3, 2 * t + 1, cq) + (slot & 7)] = lo;
+    } else {
+      K.afrag[bmain_off<BITS>(ks, slot >> 3, t, cq) + (slot & 7)] = hi;
+      K.afrag[K.afrag_set + bmain_off<BITS>(ks, slot >> 3, t, cq) + (slot & 7)] = lo;
+    }
+    // block sums: B consecutive elements of the head in B consecutive lanes
+    float sm = a;
+    const unsigned mask = B == 32 ? 0xffffffffu : (0xffffu << (tid & 16));
+#pragma unroll
+    for (int o = B / 2; o > 0; o >>= 1) sm += __shfl_xor_sync(mask, sm, o);
+    if ((f % B) == 0) K.asum[(long long)t * (L.dq / B) + f / B] = sm;
+  }
+}
+
 // A window through n decoder layers in one launch.  Per layer:
 //   D0. every CTA: 1/RMS of each row of x; all CTAs write the fragments of
 //       x / RMS(x);  grid barrier
@@ -2092,6 +2352,15 @@ __global__ void __launch_bounds__(kExpertThreads, 1)
     // D1
     dense_phase<BITS, 2>(L, sW, C, sp, rg, m, rp, buf);
     if (!grid_barrier(sW, &sp.ok) || s_abort) return;
+    if (sW.kv.k) {
+      // A0-A2: attention over each slot's KV cache
+      kv_append(L, sW, l);
+      if (!grid_barrier(sW, &sp.ok)) return;
+      kv_partials(L, sW, l, m.ring);
+      if (!grid_barrier(sW, &sp.ok)) return;
+      kv_combine<BITS>(L, sW);
+      if (!grid_barrier(sW, &sp.ok)) return;
+    }
     // D2
     dense_phase<BITS, 3>(L, sW, C, sp, rg, m, rp, buf);
     if (!grid_barrier(sW, &sp.ok) || s_abort) return;
