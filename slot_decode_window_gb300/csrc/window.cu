@@ -592,9 +592,11 @@ __device__ __forceinline__ bool grid_barrier(const WindowBufs& W, int* s_ok) {
 // partials summed in chunk order (four chunks' loads in flight at a time, so
 // every CTA gets the same bits), top-k by logit (descending, ties to the lower
 // expert), fp32 softmax over all E, and the selected experts' gate weights.
+// NI: experts per lane, ceil(E / 32) rounded up to a power of two (the
+// caller dispatches on E), so lanes scan no keys that cannot be experts.
+template <int NI>
 __device__ __forceinline__ void plan_row(const LayerDev& L, const WindowBufs& W, SPlan& sp, int t, int lane,
                                          bool pub) {
-  constexpr int NI = kMaxExperts / 32;
   const int E = L.E, k = L.k, njb = W.njb;
   float val[NI];
 #pragma unroll
@@ -774,7 +776,12 @@ __device__ __noinline__ void compute_plan(const LayerDev& L, const WindowBufs& W
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool pub = blockIdx.x == 0;
   // 1-2. row t (warp t): logits, top-k, softmax, gate weights
-  if (warp < T) plan_row(L, W, sp, warp, lane, pub);
+  if (warp < T) {
+    if (E <= 32) plan_row<1>(L, W, sp, warp, lane, pub);
+    else if (E <= 64) plan_row<2>(L, W, sp, warp, lane, pub);
+    else if (E <= 128) plan_row<4>(L, W, sp, warp, lane, pub);
+    else plan_row<8>(L, W, sp, warp, lane, pub);
+  }
   __syncthreads();
   STAMP(0, 18);
   // 3. grouping: entries ordered by expert, then by entry index.  Warps 0 and 1
@@ -1025,9 +1032,9 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
   } else if (W.kv.k) {
     // the o projection's input is the cache attention's output: its main
     // fragments stay in global memory (kv_combine wrote them in this layout);
-    // its block sums are split into hi/lo here
+    // its block sums are split into hi/lo here (the padded sum slots were
+    // cleared before the phase: dense_o_prologue)
     const int nb = L.dq / B;
-    zero_padded_sums(bs, C, nb, (nb + 15) / 16, R, paired, ctid);
     for (int i = ctid; i < R * nb; i += kConsumerThreads) {
       const int r = i / nb, blk = i - r * nb;
       __half hi, lo;
@@ -1044,7 +1051,7 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
       }
     }
   } else {
-    zero_padded_sums(bs, C, L.dq / B, (L.dq / B + 15) / 16, R, paired, ctid);
+    // (the padded sum slots were cleared before the phase: dense_o_prologue)
     // v (K = dkv): one element per thread and step; a warp covers 32
     // consecutive elements of one row (K is a multiple of 64), so block sums
     // come from lane shuffles, written for every block of the broadcast input
@@ -1978,6 +1985,26 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
   return true;
 }
 
+// Before the dense o phase (all threads): its input is dq wide, and when dq /
+// block is not a multiple of 16 the last min group has padded block slots
+// whose min fragments are zero; an earlier phase may have left a non-finite
+// sum there (0 x NaN = NaN), so they are cleared in every column of both
+// sets.  The phase stages one group (all rows) and writes only real blocks,
+// so they stay clear through it.  (Clearing them inside the staging itself
+// slowed the stack's dense phases by a sixth.)
+__device__ __noinline__ void dense_o_prologue(const LayerDev& L, const KernelCfg& C, __half* bs, int bits) {
+  const int nb = L.dq / (bits == 4 ? 32 : 16), nmk = (nb + 15) / 16, npad = nmk * 16 - nb;
+  if (npad <= 0) return;
+  const __half z = __float2half_rn(0.f);
+  for (int i = threadIdx.x; i < 16 * npad; i += blockDim.x) {
+    const int col = i / npad, blk = nb + (i - col * npad);
+    const int spos = frag_sum_pos(blk);
+    const int o = (spos >> 4) * 128 + col * 16 + ((spos >> 2) & 3) * 4 + (spos & 3);
+    bs[o] = z;
+    bs[C.bsum_halves + o] = z;
+  }
+}
+
 // One dense projection phase (2: [Wq; Wk; Wv] a, 3: x + Wo att) over all T
 // rows, its row tiles split evenly over the CTAs.
 template <int BITS, int PHASE>
@@ -2362,6 +2389,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1)
       if (!grid_barrier(sW, &sp.ok)) return;
     }
     // D2
+    dense_o_prologue(L, C, m.bs, BITS);
     dense_phase<BITS, 3>(L, sW, C, sp, rg, m, rp, buf);
     if (!grid_barrier(sW, &sp.ok) || s_abort) return;
     // M

@@ -7,8 +7,8 @@ window's positions and NaN everywhere the window must not read (positions past
 each slot's last window row, and slots with no row), so any stray read shows
 up as a non-finite output.  Routing must match the oracle bit for bit at every
 layer on rows whose fp64 router margin stays >= 1e-3; y, q and k within
-2e-3 x RMS; the entries the window appends within fp16 rounding of the
-oracle's.
+2e-3 x RMS; the entries the window appends within that tolerance plus fp16
+rounding of the oracle's.
 """
 import numpy as np
 import pytest
@@ -92,14 +92,16 @@ def _compare(wl, n_layers, slots, positions, y, out, kg, vg, ref):
             rl = np.stack([r[l][t] for t in rows])
             e = np.abs(g[l][rows].astype(np.float64) - rl).max()
             assert e <= TOL * np.sqrt(np.mean(rl * rl)), f"{name} layer {l}"
-    # the window's appended entries: within fp16 rounding of the oracle's
+    # the window's appended entries: the row's k and v (within the tolerance)
+    # rounded to fp16 (within half an fp16 step more)
     for l in range(n_layers):
         for t in rows:
             s, p = slots[t], positions[t]
             for got, want in ((kg, kcs), (vg, vcs)):
                 a = got[l, s, :, p, :].astype(np.float64)
                 b = want[l][s, :, p, :]
-                assert np.all(np.abs(a - b) <= 2.0 ** -9 * np.abs(b) + 2.0 ** -20)
+                bound = TOL * np.sqrt(np.mean(b * b)) + 2.0 ** -10 * np.abs(b)
+                assert np.all(np.abs(a - b) <= bound), f"appended entry: layer {l} row {t}"
 
 
 SMALL = wlm.Workload("stack_kv_small", 95, wlm.MoESpec(256, 8, 2, 128, 128, 4, 32), (1,), n_layers=3,
