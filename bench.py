@@ -53,8 +53,10 @@ def parse():
     p.add_argument("--no-workloads", action="store_true", help="skip the zipf and lowbit layer measurements")
     p.add_argument("--stack-steps", type=int, default=30)
     p.add_argument("--stack-layers", type=int, default=2, help="layers of the stack in --mode stack")
-    p.add_argument("--mode", choices=("full", "windows", "stack"), default="full",
-                   help="windows: only warmup + K windows at --rows (a clean launch sequence for ncu)")
+    p.add_argument("--mode", choices=("full", "windows", "stack", "head"), default="full",
+                   help="windows / stack / head: only warmup + K launches of that kernel (a clean launch "
+                        "sequence for ncu)")
+    p.add_argument("--kv", action="store_true", help="--mode stack: attend over KV caches (positions ~1000)")
     return p.parse_args()
 
 
@@ -371,13 +373,44 @@ def run_ours(args, rank, world, local_rank):
         T = args.rows
         xw = torch.from_numpy(np.stack([wlm.make_window(wls, T, seed=0, window=w) for w in range(4)])).to(dev)
         yw = torch.empty(T, wls.moe.hidden, device=dev)
+        kw = {}
+        if args.kv:
+            shape = (n, 4, wls.kv_heads, 1024, wls.head_dim)
+            kc = torch.randn(shape, device=dev).to(torch.float16)
+            vc = torch.randn(shape, device=dev).to(torch.float16)
+            stk.set_kv(kc, vc, 4, 1024)
+            kw = dict(slot=torch.tensor([0, 0, 1, 1, 2, 2, 3, 3][:T], dtype=torch.int32, device=dev),
+                      position=torch.tensor([1000, 1001] * 4, dtype=torch.int32, device=dev)[:T])
         for i in range(args.warmup + args.steps):
-            stk.forward(xw[i % 4], yw)
+            stk.forward(xw[i % 4], yw, **kw)
         stk.sync()
         if rank == 0:
             print(json.dumps({"mode": "stack", "layers": n, "T": T, "windows": args.steps}), flush=True)
         stk.close()
         win.close()
+        return
+
+    if args.mode == "head":
+        # the output head at the stack model's shape: warmup + K windows
+        win.close()
+        del layer
+        torch.cuda.empty_cache()
+        d, V, T = 2048, wlm.HEAD_VOCAB, args.rows
+        W = wlm.make_head(V, d, 4, 32, seed=0, cfg_id=4, device=str(dev))
+        head = binding.Head(W, max_rows=8)
+        del W
+        torch.cuda.empty_cache()
+        xs = torch.randn(4, T, d, device=dev)
+        pos = torch.arange(100, 100 + T, dtype=torch.int32, device=dev)
+        seed = torch.full((T,), 12345, dtype=torch.int64, device=dev)
+        temp = torch.tensor([0.0, 0.0, 0.7, 0.7, 0.0, 0.0, 1.0, 1.0][:T], device=dev)
+        fed = torch.tensor([-1, 0] * 4, dtype=torch.int32, device=dev)[:T]
+        for i in range(args.warmup + args.steps):
+            head.forward(xs[i % 4], pos, seed, temp, fed)
+        head.sync()
+        if rank == 0:
+            print(json.dumps({"mode": "head", "T": T, "windows": args.steps}), flush=True)
+        head.close()
         return
 
     if args.mode == "windows":
