@@ -58,7 +58,7 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 // default build compiles these to nothing.
 #ifdef STRATA_STAMPS
 }  // namespace
-__device__ unsigned long long g_stamps[1024][20];
+__device__ unsigned long long g_stamps[1024][32];
 namespace {
 __device__ __forceinline__ void stamp(int slot) {
   unsigned long long t;
@@ -70,8 +70,8 @@ __device__ __forceinline__ void stamp(int slot) {
     if (threadIdx.x == (tid_)) stamp(slot_); \
   } while (0)
 // per-task trace: g_trace[cta][phase][task slot][event]
-__device__ unsigned long long g_trace[1024][2][32][4];
-__device__ unsigned long long g_ptrace[1024][2][64];  // producer: chunk issue times
+__device__ unsigned long long g_trace[1024][4][32][4];
+__device__ unsigned long long g_ptrace[1024][4][64];  // producer: chunk issue times
 __device__ __forceinline__ void trace(int phase, int slot, int ev) {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -977,6 +977,7 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
     };
     // main: 16-byte pieces (ks, c, plane) of each used column
     const int per_col = nks * 4 * (S / 8);
+    TRACE(0, PHASE, 31, 0);
     for (int i = ctid; i < nsets * ncols * per_col; i += kConsumerThreads) {
       const int cs = i / per_col, rem = i - cs * per_col;
       const int set = cs / ncols, col = cs - set * ncols;
@@ -987,6 +988,7 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
       cp_async16(bm + set * C.bmain_halves + bmain_off<BITS>(ks, p, col, c),
                  row_base(r) + (long long)part * K + ks * 4 * S + c * S + p * 8);
     }
+    TRACE(0, PHASE, 31, 1);
     if constexpr (PHASE == 1) {
       // padded block slots of the last min group (blocks K/B .. 16 nmk - 1):
       // their min fragments are zero, but an earlier group may have left a
@@ -1028,7 +1030,9 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
         *reinterpret_cast<uint2*>(bs + set * C.bsum_halves + (mk * 8 + col) * 16 + c * 4) = v;
       }
     }
+    TRACE(0, PHASE, 31, 2);
     cp_async_wait_all();
+    TRACE(0, PHASE, 31, 3);
   } else if (W.kv.k) {
     // the o projection's input is the cache attention's output: its main
     // fragments stay in global memory (kv_combine wrote them in this layout);
@@ -1224,7 +1228,7 @@ __device__ bool produce(const LayerDev& L, const WindowBufs& W, const KernelCfg&
       const int stage = rp.stage;
       if (rp.n >= C.nstages && !wait_bar(&rg.empty[stage], rp.parity ^ 1u, W.err, rg.abort_flag, W.wait_cycles))
         return false;
-      if (PHASE < 2) PTRACE(PHASE, (task - pt.t0) * P.nchunks + ch);
+      PTRACE(PHASE, (task - pt.t0) * P.nchunks + ch);
       const uint32_t cbytes = (uint32_t)((ks1 - ks0) * Fmt<BITS>::kChunk), mbytes = (uint32_t)((mk1 - mk0) * 512);
       uint8_t* dst = rg.base + (size_t)stage * C.stage_bytes;
       if (P.nchunks == 1 && tbytes == P.sub_stride) {
@@ -1441,6 +1445,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
   const int sub = warp / kWPS, kg = warp % kWPS;
   GroupState gs;
   TaskWalk tw;
+  TRACE(0, PHASE, 30, 0);
   if (pt.t0 < pt.t1) tw.start(pt.t0, pt, has_shared, sp);
   for (int task = pt.t0; task < pt.t1; ++task, tw.next(pt, has_shared, sp)) {
     const Task& tk = tw.tk;
@@ -1450,7 +1455,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
     if (tk.group != gs.cur) enter_group<BITS, PHASE>(L, W, C, sp, tk, K, rg.abort_flag, bm, bs, gs);
     const int kv = (PHASE == 1 && tk.shared) ? 1 : 0;
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f}, accm2[4] = {0.f, 0.f, 0.f, 0.f};
-    if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 0);
+    TRACE(0, PHASE, task - pt.t0, 0);
     for (int ch = 0; ch < P.nchunks; ++ch) {
       const int ks0 = P.cks[kv][ch], ks1 = P.cks[kv][ch + 1];
       const int mk0 = P.cmk[kv][ch], mk1 = P.cmk[kv][ch + 1];
@@ -1459,7 +1464,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
       const int m0 = (kg * nm) / kWPS, m1 = ((kg + 1) * nm) / kWPS;
       const int stage = rp.stage;
       if (wait_bar(&rg.full[stage], rp.parity, W.err, rg.abort_flag, W.wait_cycles)) {
-        if (PHASE < 2 && ch == 0) TRACE(0, PHASE, task - pt.t0, 1);
+        if (ch == 0) TRACE(0, PHASE, task - pt.t0, 1);
         const uint8_t* st = rg.base + (size_t)stage * C.stage_bytes + sub * P.sub_stride;
         if (PHASE == 3 && !W.kv.k) {  // the length-one reading: v's fragments, k-steps remapped
           if (gs.paired)
@@ -1487,11 +1492,11 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
       if (lane == 0) mbar_arrive(&rg.empty[stage]);
       rp.advance(C.nstages);
     }
-    if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 2);
+    TRACE(0, PHASE, task - pt.t0, 2);
     float4* rb = red + buf * (kConsumerWarps * 32);
     rb[warp * 32 + lane] = gs.paired ? partials<true>(acc, accm, accm2) : partials<false>(acc, accm, accm2);
     consumer_sync();  // all 16 warps: the ring path's warps stay in step
-    if (PHASE < 2) TRACE(0, PHASE, task - pt.t0, 3);
+    TRACE(0, PHASE, task - pt.t0, 3);
 
     constexpr int kMT = PHASE == 0 ? NS / 2 : NS;
     task_epilogue<BITS, PHASE, NS>(L, W, sp, rb, tk, gs, (tid + 32 * (task & (kConsumerWarps - 1))) & (kConsumerThreads - 1),
@@ -2371,14 +2376,19 @@ __global__ void __launch_bounds__(kExpertThreads, 1)
     }
     for (int i = tid; i < 2 * kMaxExperts; i += blockDim.x) (&sp.wcnt[0][0])[i] = 0;
     __syncthreads();
+    STAMP(0, 20);
     const LayerDev& L = sL;
     // D0
     row_rinv(sW.x, sW.T, L.d, s_rinv);
     write_x_frags<BITS>(L, sW);
+    STAMP(0, 21);
     if (!grid_barrier(sW, &sp.ok)) return;
+    STAMP(0, 22);
     // D1
     dense_phase<BITS, 2>(L, sW, C, sp, rg, m, rp, buf);
+    STAMP(0, 23);
     if (!grid_barrier(sW, &sp.ok) || s_abort) return;
+    STAMP(0, 24);
     if (sW.kv.k) {
       // A0-A2: attention over each slot's KV cache
       kv_append(L, sW, l);
@@ -2391,7 +2401,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1)
     // D2
     dense_o_prologue(L, C, m.bs, BITS);
     dense_phase<BITS, 3>(L, sW, C, sp, rg, m, rp, buf);
+    STAMP(0, 25);
     if (!grid_barrier(sW, &sp.ok) || s_abort) return;
+    STAMP(0, 26);
     // M
     if (tid == 0) {
       sW.x = sW.x1;
@@ -2400,13 +2412,18 @@ __global__ void __launch_bounds__(kExpertThreads, 1)
     __syncthreads();
     row_rinv(sW.x, sW.T, L.d, s_rinv);
     router_stage<BITS>(L, sW, reinterpret_cast<float*>(m.ring));
+    STAMP(0, 27);
     if (!grid_barrier(sW, &sp.ok)) return;
+    STAMP(0, 28);
     if (!moe_block<BITS>(L, sW, C, sp, rg, m, rp, buf)) return;
     if (sW.T >= kGridCombineRows) {
       if (!grid_barrier(sW, &sp.ok) || s_abort) return;
+      STAMP(0, 29);
       combine_all(L, sW);
     }
+    STAMP(0, 30);
     if (!grid_barrier(sW, &sp.ok) || s_abort) return;
+    STAMP(0, 31);
   }
 }
 
@@ -2983,16 +3000,16 @@ cudaError_t launch_stack(const LayerDev* layers, int n_layers, int bits, const W
 #ifdef STRATA_STAMPS
 // Timing builds only: copy the stage timestamps of the first n CTAs to host.
 extern "C" int strata_probe_stamps(void* host, int n) {
-  return (int)cudaMemcpyFromSymbol(host, strata::g_stamps, (size_t)n * 20 * sizeof(unsigned long long));
+  return (int)cudaMemcpyFromSymbol(host, strata::g_stamps, (size_t)n * 32 * sizeof(unsigned long long));
 }
 extern "C" int strata_probe_trace(void* host, int n) {
-  return (int)cudaMemcpyFromSymbol(host, strata::g_trace, (size_t)n * 2 * 32 * 4 * sizeof(unsigned long long));
+  return (int)cudaMemcpyFromSymbol(host, strata::g_trace, (size_t)n * 4 * 32 * 4 * sizeof(unsigned long long));
 }
 extern "C" int strata_probe_ptrace(void* host, int n) {
-  return (int)cudaMemcpyFromSymbol(host, strata::g_ptrace, (size_t)n * 2 * 64 * sizeof(unsigned long long));
+  return (int)cudaMemcpyFromSymbol(host, strata::g_ptrace, (size_t)n * 4 * 64 * sizeof(unsigned long long));
 }
 extern "C" int strata_probe_trace_clear() {
-  static unsigned long long zero[1024 * 2 * 32 * 4];
+  static unsigned long long zero[1024 * 4 * 32 * 4];
   return (int)cudaMemcpyToSymbol(strata::g_trace, zero, sizeof(zero));
 }
 #endif
