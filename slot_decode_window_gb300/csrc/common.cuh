@@ -131,7 +131,7 @@ struct WindowBufs {
   int* out_topk_idx; float* out_topk_w; int* out_counts; int* out_offsets;
   int* out_entries; int* out_distinct; int* out_ndistinct;
   // workspace
-  __half* xfrag;           // [kMaxRows][frag(d)]
+  __half* xfrag;           // x fragments of the T rows as one B image (16 d + 256 nmk halves)
   // h = silu(Wg x) * (Wu x) of each routed entry, written by the gate/up
   // epilogue already in activation-fragment form: fp16 hi then lo parts of
   // F elements each (the x-fragment main layout), plus fp32 sums of h over
@@ -157,6 +157,8 @@ struct WindowBufs {
   const float* resid;      // [T][d] added to y in the combine
   float* v;                // [kMaxRows][dkv] value projection
   float* x1;               // [kMaxRows][d] x + Wo att
+  __half* vimg;            // the o phase's length-one B operand: v as one B image (16 dkv halves), or null
+  float* vsum;             // [kMaxRows][dkv / block] v's block sums (zeroed in D0, added by D1's epilogue)
   float* q_out;            // [T][dq] or null
   float* k_out;            // [T][dkv] or null
 };

@@ -6,8 +6,10 @@ namespace strata {
 
 constexpr int kRouterCols = 512;  // columns per router partial-logit chunk
 
-// Shared-memory plan of the window kernel for one layer shape.
-KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit);
+// Shared-memory plan of the window kernel for one layer shape.  grid: the
+// CTAs a decoder stack launches with (its dense phases are cut for the task
+// width they run at there), or 0 for a plain window.
+KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit, int grid);
 // The same with the warp-streamed path (C.direct) where it is the faster one
 // and the shape allows it.
 KernelCfg window_cfg_direct(const LayerDev& L, int max_rows, int smem_limit);

@@ -160,8 +160,10 @@ strata_status strata_stack_create(int32_t n_layers, const strata_moe_desc* moe, 
   }
 
   // ---- residual-stream buffers; the rest of the workspace is layer 0's ----
+  // v, x1, two ping-pong residual planes, then v's block sums and v's B image
   const size_t n_v = (size_t)kMaxRows * dkv, n_x = (size_t)kMaxRows * d;
-  if (cudaMalloc(&s->extra, (n_v + 3 * n_x) * sizeof(float)) != cudaSuccess) {
+  const size_t n_vs = (size_t)kMaxRows * (dkv / 16), n_vi = (size_t)8 * dkv;  // n_vi floats = 16 dkv halves
+  if (cudaMalloc(&s->extra, (n_v + 3 * n_x + n_vs + n_vi) * sizeof(float)) != cudaSuccess) {
     cudaGetLastError();
     free_stack(s);
     return STRATA_ENOMEM;
@@ -169,6 +171,8 @@ strata_status strata_stack_create(int32_t n_layers, const strata_moe_desc* moe, 
   s->W = h0->W;
   s->W.v = s->extra;
   s->W.x1 = s->extra + n_v;
+  s->W.vsum = s->extra + n_v + 3 * n_x;
+  s->W.vimg = reinterpret_cast<__half*>(s->W.vsum + n_vs);
 
   int optin = 0;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h0->device) != cudaSuccess ||
@@ -177,7 +181,7 @@ strata_status strata_stack_create(int32_t n_layers, const strata_moe_desc* moe, 
     free_stack(s);
     return STRATA_ECUDA;
   }
-  s->cfg = window_cfg(L0, moe->max_rows, optin - 12288);
+  s->cfg = window_cfg(L0, moe->max_rows, optin - 12288, h0->nsm);
   if (s->cfg.nstages < 2) {
     free_stack(s);
     return STRATA_EUNSUPPORTED;

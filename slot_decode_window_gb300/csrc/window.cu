@@ -356,12 +356,39 @@ __device__ __forceinline__ float unord_f32(unsigned u) {
 // ---------------------------------------------------------------------------
 // stage R: router partial logits and x fragments (all threads of all CTAs)
 // ---------------------------------------------------------------------------
+// The x fragments of a window live in global memory as the image of the
+// shared-memory B operand of a group holding all T rows in order (the shared
+// expert's group, and every dense phase's): set s of the main part at
+// s * 8d halves, laid out as bmain_off; the sums after both sets, set s at
+// 16d + s * 128 nmk halves, laid out as the B sums.  Rows > 4 use two sets
+// (hi, lo); otherwise set 0 holds columns 2t (hi) and 2t + 1 (lo).  A group
+// of all rows then stages with a plain copy; any other group gathers its
+// rows' 16-byte pieces from their columns.
+struct XImg {
+  int set, col;  // row t's place for part (0: hi, 1: lo)
+  __device__ __forceinline__ XImg(int T, int t, int part) {
+    set = T <= 4 ? 0 : part;
+    col = T <= 4 ? 2 * t + part : t;
+  }
+};
+// Element with fragment offset off (frag_main_pos) of row t, part part.
+template <int BITS>
+__device__ __forceinline__ long long ximg_main(int T, int d, int t, int part, int off) {
+  constexpr int S = Fmt<BITS>::kBHalves;
+  const XImg q(T, t, part);
+  return (long long)q.set * 8 * d + bmain_off<BITS>(off / (4 * S), (off % S) >> 3, q.col, (off / S) & 3) + (off & 7);
+}
+// Block sum with sum offset soff (frag_sum_pos) of row t, part part.
+__device__ __forceinline__ long long ximg_sum(int T, int d, int nmk, int t, int part, int soff) {
+  const XImg q(T, t, part);
+  return 16LL * d + (long long)q.set * 128 * nmk + ((soff >> 4) * 8 + q.col) * 16 + ((soff >> 2) & 3) * 4 + (soff & 3);
+}
+
 template <int BITS>
 __device__ void write_x_frags(const LayerDev& L, const WindowBufs& W) {
   constexpr int B = Fmt<BITS>::kBlock;
   const int d = L.d;
   const int nmk = (d / B + 15) / 16;
-  const long long fh = frag_halves(d, nmk);
   const long long n_el = (long long)W.T * d;  // a multiple of 64: warps never straddle a block or a row
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -371,15 +398,14 @@ __device__ void write_x_frags(const LayerDev& L, const WindowBufs& W) {
     const bool in = i < n_el;
     const int t = in ? (int)(i / d) : 0, j = in ? (int)(i % d) : 0;
     const float v = in ? (W.rinv ? W.x[i] * W.rinv[t] : W.x[i]) : 0.f;
-    __half* base = W.xfrag + t * fh;
     if (in) {
       int off;
       float f;
       frag_main_pos<BITS>(j, off, f);
       __half hi, lo;
       split_hi_lo(v * f, hi, lo);
-      base[off] = hi;
-      base[d + off] = lo;
+      W.xfrag[ximg_main<BITS>(W.T, d, t, 0, off)] = hi;
+      W.xfrag[ximg_main<BITS>(W.T, d, t, 1, off)] = lo;
     }
     float s = v;
 #pragma unroll
@@ -388,8 +414,8 @@ __device__ void write_x_frags(const LayerDev& L, const WindowBufs& W) {
       __half hi, lo;
       split_hi_lo(s, hi, lo);
       const int off = frag_sum_pos(j / B);
-      base[2 * d + off] = hi;
-      base[2 * d + nmk * 16 + off] = lo;
+      W.xfrag[ximg_sum(W.T, d, nmk, t, 0, off)] = hi;
+      W.xfrag[ximg_sum(W.T, d, nmk, t, 1, off)] = lo;
     }
   }
 }
@@ -462,7 +488,6 @@ __device__ __noinline__ void router_stage(const LayerDev& L, const WindowBufs& W
   const int nwarps = blockDim.x >> 5;
   const bool spread = G >= njb;  // several CTAs per chunk (always, for the shapes here)
   const int nmk = (d / B + 15) / 16;
-  const long long fh = frag_halves(d, nmk);
   for (int jb = spread ? (int)blockIdx.x % njb : (int)blockIdx.x; jb < njb; jb += spread ? njb : G) {
     const int cpc = spread ? G / njb + (jb < G % njb ? 1 : 0) : 1;  // CTAs on this chunk
     const int ci = spread ? (int)blockIdx.x / njb : 0;              // this CTA among them
@@ -521,22 +546,21 @@ __device__ __noinline__ void router_stage(const LayerDev& L, const WindowBufs& W
     for (int u = ci + cpc * warp; u < nu; u += cpc * nwarps) {
       const int t = u / upr, jj = (u - t * upr) * 32 + lane, j = j0 + jj;
       const float v = W.rinv ? xs[t * kRouterCols + jj] * W.rinv[t] : xs[t * kRouterCols + jj];
-      __half* base = W.xfrag + t * fh;
       int off;
       float f;
       frag_main_pos<BITS>(j, off, f);
       __half hi, lo;
       split_hi_lo(v * f, hi, lo);
-      base[off] = hi;
-      base[d + off] = lo;
+      W.xfrag[ximg_main<BITS>(T, d, t, 0, off)] = hi;
+      W.xfrag[ximg_main<BITS>(T, d, t, 1, off)] = lo;
       float sm = v;
 #pragma unroll
       for (int o = B / 2; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
       if ((j % B) == 0) {
         split_hi_lo(sm, hi, lo);
         const int soff = frag_sum_pos(j / B);
-        base[2 * d + soff] = hi;
-        base[2 * d + nmk * 16 + soff] = lo;
+        W.xfrag[ximg_sum(T, d, nmk, t, 0, soff)] = hi;
+        W.xfrag[ximg_sum(T, d, nmk, t, 1, soff)] = lo;
       }
     }
   }
@@ -964,20 +988,63 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
   const bool paired = R <= 4;
   const int nsets = paired ? 1 : 2;
   const int ncols = paired ? 2 * R : R;
-  if constexpr (PHASE != 3) {
-    // the source of column col's part (hi or lo): one row of fragments
-    const long long fh = frag_halves(K, nmk);
-    auto row_base = [&](int r) -> const __half* {
-      if constexpr (PHASE == 1) {
-        return is_shared ? W.shfrag + (long long)r * 2 * L.Fs : W.hfrag + (long long)sp.entries[ent_off + r] * 2 * L.F;
-      } else {
-        const int xrow = (PHASE == 2 || is_shared) ? r : sp.entries[ent_off + r] / L.k;
-        return W.xfrag + xrow * fh;
+  if constexpr (PHASE == 0 || PHASE == 2) {
+    // x fragments (the window's B image, K = d)
+    TRACE(0, PHASE, 31, 0);
+    const int T = W.T;
+    if (PHASE == 2 || is_shared) {
+      // all T rows in order: the image is this group's B as it stands
+      const int per_set = 8 * K / 8;  // 16-byte pieces of one set's main part
+      for (int i = ctid; i < nsets * per_set; i += kConsumerThreads) {
+        const int set = i >= per_set ? 1 : 0, q = i - set * per_set;
+        cp_async16(bm + set * C.bmain_halves + q * 8, W.xfrag + (long long)set * 8 * K + q * 8);
       }
+      TRACE(0, PHASE, 31, 1);
+      const int sum_set = 32 * nmk;  // 8-byte pieces of one set's sums
+      for (int i = ctid; i < nsets * sum_set; i += kConsumerThreads) {
+        const int set = i >= sum_set ? 1 : 0, q = i - set * sum_set;
+        *reinterpret_cast<uint2*>(bs + set * C.bsum_halves + q * 4) =
+            __ldcg(reinterpret_cast<const uint2*>(W.xfrag + 16LL * K + (long long)set * 128 * nmk + q * 4));
+      }
+    } else {
+      // an expert's rows: each column's 16-byte pieces from its row's column
+      // of the image
+      const int per_col = nks * 4 * (S / 8);
+      for (int i = ctid; i < nsets * ncols * per_col; i += kConsumerThreads) {
+        const int cs = i / per_col, rem = i - cs * per_col;
+        const int set = cs / ncols, col = cs - set * ncols;
+        const int r = paired ? (col >> 1) : col;
+        const int part = paired ? (col & 1) : set;
+        const int ks = rem / (4 * (S / 8)), cp = rem - ks * 4 * (S / 8);
+        const int c = cp / (S / 8), p = cp - c * (S / 8);
+        const XImg q(T, sp.entries[ent_off + r] / L.k, part);
+        cp_async16(bm + set * C.bmain_halves + bmain_off<BITS>(ks, p, col, c),
+                   W.xfrag + (long long)q.set * 8 * K + bmain_off<BITS>(ks, p, q.col, c));
+      }
+      TRACE(0, PHASE, 31, 1);
+      for (int i = ctid; i < nsets * ncols * nmk * 4; i += kConsumerThreads) {
+        const int cs = i / (nmk * 4), rem = i - cs * nmk * 4;
+        const int set = cs / ncols, col = cs - set * ncols;
+        const int r = paired ? (col >> 1) : col;
+        const int part = paired ? (col & 1) : set;
+        const int mk = rem >> 2, c = rem & 3;
+        const XImg q(T, sp.entries[ent_off + r] / L.k, part);
+        const uint2 v = __ldcg(reinterpret_cast<const uint2*>(W.xfrag + 16LL * K + (long long)q.set * 128 * nmk +
+                                                              (mk * 8 + q.col) * 16 + c * 4));
+        *reinterpret_cast<uint2*>(bs + set * C.bsum_halves + (mk * 8 + col) * 16 + c * 4) = v;
+      }
+    }
+    TRACE(0, PHASE, 31, 2);
+    cp_async_wait_all();
+    TRACE(0, PHASE, 31, 3);
+  } else if constexpr (PHASE == 1) {
+    // h fragments (one row of fragments per entry, or per row for the shared
+    // expert), and the block sums formed from their 16-element partial sums
+    auto row_base = [&](int r) -> const __half* {
+      return is_shared ? W.shfrag + (long long)r * 2 * L.Fs : W.hfrag + (long long)sp.entries[ent_off + r] * 2 * L.F;
     };
     // main: 16-byte pieces (ks, c, plane) of each used column
     const int per_col = nks * 4 * (S / 8);
-    TRACE(0, PHASE, 31, 0);
     for (int i = ctid; i < nsets * ncols * per_col; i += kConsumerThreads) {
       const int cs = i / per_col, rem = i - cs * per_col;
       const int set = cs / ncols, col = cs - set * ncols;
@@ -988,49 +1055,33 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
       cp_async16(bm + set * C.bmain_halves + bmain_off<BITS>(ks, p, col, c),
                  row_base(r) + (long long)part * K + ks * 4 * S + c * S + p * 8);
     }
-    TRACE(0, PHASE, 31, 1);
-    if constexpr (PHASE == 1) {
-      // padded block slots of the last min group (blocks K/B .. 16 nmk - 1):
-      // their min fragments are zero, but an earlier group may have left a
-      // non-finite sum there (0 x NaN = NaN), so they are cleared for every
-      // column this group uses
-      zero_padded_sums(bs, C, K / B, nmk, R, paired, ctid);
-      // block sums from the 16-element partial sums, split into hi/lo
-      constexpr int kParts = B / 16;
-      for (int i = ctid; i < R * (K / B); i += kConsumerThreads) {
-        const int r = i / (K / B), blk = i - r * (K / B);
-        const float* hs = is_shared ? W.shsum + (long long)r * (L.Fs / 16)
-                                    : W.hsum + (long long)sp.entries[ent_off + r] * (L.F / 16);
-        float sum = 0.f;
+    // padded block slots of the last min group (blocks K/B .. 16 nmk - 1):
+    // their min fragments are zero, but an earlier group may have left a
+    // non-finite sum there (0 x NaN = NaN), so they are cleared for every
+    // column this group uses
+    zero_padded_sums(bs, C, K / B, nmk, R, paired, ctid);
+    // block sums from the 16-element partial sums, split into hi/lo
+    constexpr int kParts = B / 16;
+    for (int i = ctid; i < R * (K / B); i += kConsumerThreads) {
+      const int r = i / (K / B), blk = i - r * (K / B);
+      const float* hs = is_shared ? W.shsum + (long long)r * (L.Fs / 16)
+                                  : W.hsum + (long long)sp.entries[ent_off + r] * (L.F / 16);
+      float sum = 0.f;
 #pragma unroll
-        for (int j = 0; j < kParts; ++j) sum += __ldcg(hs + blk * kParts + j);
-        __half hi, lo;
-        split_hi_lo(sum, hi, lo);
-        const int spos = frag_sum_pos(blk);
-        const int mk = spos >> 4, c = (spos >> 2) & 3, slot = spos & 3;
-        const int o = mk * 128 + c * 4 + slot;
-        if (paired) {
-          bs[o + (2 * r) * 16] = hi;
-          bs[o + (2 * r + 1) * 16] = lo;
-        } else {
-          bs[o + r * 16] = hi;
-          bs[C.bsum_halves + o + r * 16] = lo;
-        }
-      }
-    } else {
-      // sums: 8-byte pieces (mk, c)
-      for (int i = ctid; i < nsets * ncols * nmk * 4; i += kConsumerThreads) {
-        const int cs = i / (nmk * 4), rem = i - cs * nmk * 4;
-        const int set = cs / ncols, col = cs - set * ncols;
-        const int r = paired ? (col >> 1) : col;
-        const int part = paired ? (col & 1) : set;
-        const int mk = rem >> 2, c = rem & 3;
-        const uint2 v = __ldcg(reinterpret_cast<const uint2*>(row_base(r) + 2LL * K + (long long)part * 16 * nmk +
-                                                              mk * 16 + c * 4));
-        *reinterpret_cast<uint2*>(bs + set * C.bsum_halves + (mk * 8 + col) * 16 + c * 4) = v;
+      for (int j = 0; j < kParts; ++j) sum += __ldcg(hs + blk * kParts + j);
+      __half hi, lo;
+      split_hi_lo(sum, hi, lo);
+      const int spos = frag_sum_pos(blk);
+      const int mk = spos >> 4, c = (spos >> 2) & 3, slot = spos & 3;
+      const int o = mk * 128 + c * 4 + slot;
+      if (paired) {
+        bs[o + (2 * r) * 16] = hi;
+        bs[o + (2 * r + 1) * 16] = lo;
+      } else {
+        bs[o + r * 16] = hi;
+        bs[C.bsum_halves + o + r * 16] = lo;
       }
     }
-    TRACE(0, PHASE, 31, 2);
     cp_async_wait_all();
     TRACE(0, PHASE, 31, 3);
   } else if (W.kv.k) {
@@ -1055,57 +1106,38 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
       }
     }
   } else {
-    // (the padded sum slots were cleared before the phase: dense_o_prologue)
-    // v (K = dkv): one element per thread and step; a warp covers 32
-    // consecutive elements of one row (K is a multiple of 64), so block sums
-    // come from lane shuffles, written for every block of the broadcast input
-    // that repeats that v block
-    for (int i0 = 0; i0 < R * K; i0 += kConsumerThreads) {
-      const int i = i0 + ctid;
-      const bool in = i < R * K;
-      const int r = in ? i / K : 0, f = in ? i - r * K : 0;
-      float h = 0.f;
-      if (in) {
-        h = __ldcg(W.v + (long long)r * L.dkv + f);
-        int off;
-        float fac;
-        frag_main_pos<BITS>(f, off, fac);
-        const int ks = off / (4 * S), c = (off / S) & 3, slot = off % S;
-        __half hi, lo;
-        split_hi_lo(h * fac, hi, lo);
-        const int o = bmain_off<BITS>(ks, slot >> 3, 0, c) + (slot & 7);
+    // the length-one reading: v's fragments as the q/k/v epilogue left them
+    // in the window's B image (K = dkv), and its block sums split into hi/lo,
+    // each written for every block of the broadcast input that repeats that v
+    // block (the padded sum slots were cleared before the phase:
+    // dense_o_prologue)
+    for (int i = ctid; i < nsets * K; i += kConsumerThreads) {  // K 16-byte pieces per set
+      const int set = i >= K ? 1 : 0, q = i - set * K;
+      cp_async16(bm + set * C.bmain_halves + q * 8, W.vimg + (long long)set * 8 * K + q * 8);
+    }
+    const int nbv = K / B;
+    const int bph = (1 << L.kph_log2) * Fmt<BITS>::kBlocksPerKstep;
+    const int ncopy = 1 << (L.kpg_log2 - L.kph_log2);
+    for (int i = ctid; i < R * nbv; i += kConsumerThreads) {
+      const int r = i / nbv, vb = i - r * nbv;
+      __half hi, lo;
+      split_hi_lo(__ldcg(W.vsum + (long long)r * nbv + vb), hi, lo);
+      // v block vb = (kv group, block in head) -> broadcast blocks (group * G + head) * bph + j
+      const int grp = vb / bph, j = vb - grp * bph;
+      for (int hc = 0; hc < ncopy; ++hc) {
+        const int spos = frag_sum_pos((grp * ncopy + hc) * bph + j);
+        const int mk = spos >> 4, c = (spos >> 2) & 3, slot = spos & 3;
+        const int o = mk * 128 + c * 4 + slot;
         if (paired) {
-          bm[o + (2 * r) * 32] = hi;
-          bm[o + (2 * r + 1) * 32] = lo;
+          bs[o + (2 * r) * 16] = hi;
+          bs[o + (2 * r + 1) * 16] = lo;
         } else {
-          bm[o + r * 32] = hi;
-          bm[C.bmain_halves + o + r * 32] = lo;
-        }
-      }
-      float s = h;
-#pragma unroll
-      for (int o = B / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (in && (f % B) == 0) {
-        __half hi, lo;
-        split_hi_lo(s, hi, lo);
-        // v block vb = (kv group, block in head) -> broadcast blocks (group * G + head) * bph + j
-        const int bph = (1 << L.kph_log2) * Fmt<BITS>::kBlocksPerKstep;
-        const int ncopy = 1 << (L.kpg_log2 - L.kph_log2);
-        const int vb = f / B, grp = vb / bph, j = vb - grp * bph;
-        for (int hc = 0; hc < ncopy; ++hc) {
-          const int spos = frag_sum_pos((grp * ncopy + hc) * bph + j);
-          const int mk = spos >> 4, c = (spos >> 2) & 3, slot = spos & 3;
-          const int o = mk * 128 + c * 4 + slot;
-          if (paired) {
-            bs[o + (2 * r) * 16] = hi;
-            bs[o + (2 * r + 1) * 16] = lo;
-          } else {
-            bs[o + r * 16] = hi;
-            bs[C.bsum_halves + o + r * 16] = lo;
-          }
+          bs[o + r * 16] = hi;
+          bs[C.bsum_halves + o + r * 16] = lo;
         }
       }
     }
+    cp_async_wait_all();
   }
 }
 
@@ -1420,7 +1452,27 @@ __device__ __forceinline__ void task_epilogue(const LayerDev& L, const WindowBuf
           if (W.k_out) W.k_out[(long long)r * L.dkv + drow - L.dq] = v;
           if (W.kv.kbuf) W.kv.kbuf[(long long)r * L.dkv + drow - L.dq] = v;
         } else {
-          W.v[(long long)r * L.dkv + drow - L.dq - L.dkv] = v;
+          const int f = drow - L.dq - L.dkv;
+          W.v[(long long)r * L.dkv + f] = v;
+          if (W.vimg && !W.kv.k) {
+            // the length-one o phase's B operand: v's fragments in the
+            // window's B image, and v's block sums (a 16-row tile holds half
+            // a 4-bit block or one 2-bit block: at most two adds onto zero,
+            // so the sum does not depend on their order)
+            constexpr int B = Fmt<BITS>::kBlock;
+            int off;
+            float fac;
+            frag_main_pos<BITS>(f, off, fac);
+            __half hi, lo;
+            split_hi_lo(v * fac, hi, lo);
+            W.vimg[ximg_main<BITS>(W.T, L.dkv, r, 0, off)] = hi;
+            W.vimg[ximg_main<BITS>(W.T, L.dkv, r, 1, off)] = lo;
+            const unsigned half_mask = 0xffffu << (threadIdx.x & 16);
+            float ps = v;
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) ps += __shfl_xor_sync(half_mask, ps, o);
+            if (row == 0) atomicAdd(W.vsum + (long long)r * (L.dkv / B) + f / B, ps);
+          }
         }
       } else if constexpr (PHASE == 3) {
         W.x1[(long long)r * L.d + drow] = W.x[(long long)r * L.d + drow] + v;
@@ -2381,6 +2433,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1)
     // D0
     row_rinv(sW.x, sW.T, L.d, s_rinv);
     write_x_frags<BITS>(L, sW);
+    if (blockIdx.x == 0 && sW.vimg && !sW.kv.k) {  // v's block sums start at zero (D1 adds into them)
+      const int n = sW.T * (L.dkv / Fmt<BITS>::kBlock);
+      for (int i = tid; i < n; i += blockDim.x) sW.vsum[i] = 0.f;
+    }
     STAMP(0, 21);
     if (!grid_barrier(sW, &sp.ok)) return;
     STAMP(0, 22);
@@ -2746,7 +2802,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) head_kernel(LayerDev L, Win
 // gate/up need >= 2) and the fewest k-chunks per tile that fit the stage
 // budget, scored by k-steps per warp per chunk (each chunk costs one wait and
 // one release per warp).
-static PhaseCfg phase_cfg(int phase, int bits, int Kv0, int Kv1, int stage_budget, int& stage_bytes) {
+static PhaseCfg phase_cfg(int phase, int bits, int Kv0, int Kv1, int stage_budget, int& stage_bytes, int ns_only = 0) {
   const int kstep = bits == 4 ? 64 : 128, block = bits == 4 ? 32 : 16, chunk = bits == 4 ? 576 : 768;
   const int Kmax = Kv0 > Kv1 ? Kv0 : Kv1;
   const int nks = Kmax / kstep, nmk = (Kmax / block + 15) / 16;
@@ -2755,6 +2811,7 @@ static PhaseCfg phase_cfg(int phase, int bits, int Kv0, int Kv1, int stage_budge
   int best_score = -1;
   stage_bytes = 0;
   for (int ns = kMaxSub; ns >= ns_min; ns >>= 1) {
+    if (ns_only && ns != ns_only) continue;
     const int wps = kConsumerWarps / ns;
     for (int nc = 1; nc <= nks && nc <= kMaxChunks; ++nc) {
       const int cks = (nks + nc - 1) / nc, cmk = (nmk + nc - 1) / nc;
@@ -2778,8 +2835,8 @@ static PhaseCfg phase_cfg(int phase, int bits, int Kv0, int Kv1, int stage_budge
     const int cks = (nks + best.nchunks - 1) / best.nchunks, cmk = (nmk + best.nchunks - 1) / best.nchunks;
     best.sub_stride = cks * chunk + cmk * 512;
     best.mins_off = cks * chunk;
-    best.max_sub = ns_min;
-    stage_bytes = ns_min * best.sub_stride;
+    best.max_sub = ns_only ? ns_only : ns_min;
+    stage_bytes = best.max_sub * best.sub_stride;
   }
   for (int v = 0; v < 2; ++v) {
     const int K = v == 0 ? Kv0 : Kv1;
@@ -2792,7 +2849,16 @@ static PhaseCfg phase_cfg(int phase, int bits, int Kv0, int Kv1, int stage_budge
   return best;
 }
 
-KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit) {
+// The task width (row tiles per task) of a dense phase over `tiles` row
+// tiles on `grid` CTAs: the widest of 4, 2, 1 that divides the tiles and
+// still gives every CTA two tasks -- the rule dense_phase applies.
+static int dense_width(int tiles, int grid) {
+  int mt = kMaxSub;
+  while (mt > 1 && (tiles % mt != 0 || tiles / mt < 2 * grid)) mt >>= 1;
+  return mt;
+}
+
+KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit, int grid) {
   KernelCfg C{};
   const int bits = L.bits;
   const int block = bits == 4 ? 32 : 16;
@@ -2812,10 +2878,15 @@ KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit) {
   C.ph[0] = phase_cfg(0, bits, L.d, L.d, budget, sb0);
   C.ph[1] = phase_cfg(1, bits, L.F, L.Fs > 0 ? L.Fs : L.F, budget, sb1);
   C.stage_bytes = sb0 > sb1 ? sb0 : sb1;
-  if (L.dq > 0) {  // decoder layer: the dense q/k/v and o phases
+  if (L.dq > 0) {
+    // decoder layer: the dense q/k/v and o phases, cut into chunks for the
+    // task width they run at on this grid (a chunking made for 4-tile tasks
+    // leaves a 1-tile task with a quarter-full stage and more waits)
     int sb2 = 0, sb3 = 0;
-    C.ph[2] = phase_cfg(1, bits, L.d, L.d, budget, sb2);
-    C.ph[3] = phase_cfg(1, bits, L.dq, L.dq, budget, sb3);
+    const int w2 = grid > 0 ? dense_width((L.dq + 2 * L.dkv) / 16, grid) : 0;
+    const int w3 = grid > 0 ? dense_width(L.d / 16, grid) : 0;
+    C.ph[2] = phase_cfg(1, bits, L.d, L.d, budget, sb2, w2);
+    C.ph[3] = phase_cfg(1, bits, L.dq, L.dq, budget, sb3, w3);
     if (sb2 > C.stage_bytes) C.stage_bytes = sb2;
     if (sb3 > C.stage_bytes) C.stage_bytes = sb3;
   }
@@ -2831,7 +2902,7 @@ KernelCfg window_cfg(const LayerDev& L, int max_rows, int smem_limit) {
 // k-step of every task (phase 0: K = d over up to 8 warps; phase 1: K = F or
 // Fs over up to 8 warps) and the down matrix splits into 2-tile tasks.
 KernelCfg window_cfg_direct(const LayerDev& L, int max_rows, int smem_limit) {
-  KernelCfg C = window_cfg(L, max_rows, smem_limit);
+  KernelCfg C = window_cfg(L, max_rows, smem_limit, 0);
   const int kstep = L.bits == 4 ? 64 : 128;
   // measured: faster than the ring for 2-bit layers (their k-steps carry
   // twice the arithmetic) and for 4-bit layers whose wide activations leave a
@@ -2915,7 +2986,7 @@ KernelCfg head_cfg(int d, int bits, int max_rows, int smem_limit) {
   L.F = d;
   L.Fs = 0;
   L.bits = bits;
-  KernelCfg C = window_cfg(L, max_rows, smem_limit);
+  KernelCfg C = window_cfg(L, max_rows, smem_limit, 0);
   const int fixed = C.total_bytes - C.nstages * C.stage_bytes;
   const int ring = smem_limit - fixed;
   int sb2 = 0;
