@@ -1555,6 +1555,7 @@ __device__ void consume(const LayerDev& L, const WindowBufs& W, const KernelCfg&
                                    kMT * 16 * gs.R, kConsumerThreads);
     buf ^= 1;
   }
+  TRACE(0, PHASE, 30, 1);
   if (PHASE == 0) {
     // publish this CTA's finished gate/up tasks: one fence, then per-group counts
     __threadfence();
@@ -2094,6 +2095,7 @@ __device__ __forceinline__ void dense_phase(const LayerDev& L, const WindowBufs&
   if (ns == 4) consume<BITS, PHASE, 4>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
   else if (ns == 2) consume<BITS, PHASE, 2>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
   else consume<BITS, PHASE, 1>(L, W, C, sp, rg, m.bm, m.bs, m.red, rp, buf);
+  TRACE(0, PHASE, 30, 2);
 }
 
 }  // namespace
@@ -2570,6 +2572,22 @@ __device__ __forceinline__ float chunk_weight(const float* lg, int a, int b, flo
   return s;
 }
 
+// The slices' weight sums of row t in slice (CTA) order, one running fp32
+// sum: warp t loads the G sums into shared memory (all lanes, one round trip),
+// then lane 0 adds them one after another; the total goes to every lane.  The
+// chain is the same arithmetic wherever it runs, so every CTA gets the same
+// total and the same slice boundaries.
+__device__ __forceinline__ float slice_total(const float* part_sum, int t, int G, float* s_row, int lane) {
+  for (int q = lane; q < G; q += 32) s_row[q] = __ldcg(part_sum + q * kMaxRows + t);
+  __syncwarp();
+  float Z = 0.f;
+  if (lane == 0) {
+#pragma unroll 8
+    for (int q = 0; q < G; ++q) Z = __fadd_rn(Z, s_row[q]);
+  }
+  return __shfl_sync(0xffffffffu, Z, 0);
+}
+
 // The token of every row from the logits [T][V] (all CTAs; ends with CTA 0
 // writing tokens and the slots' emitted counts).
 //   greedy rows (temperature <= 0): the argmax, ties to the lower token;
@@ -2593,6 +2611,7 @@ __device__ __noinline__ bool head_select(const WindowBufs& W, const HeadArgs& H,
   float* s_w = reinterpret_cast<float*>(s_cs + kMaxRows);          // [32]
   float* s_incl = s_w + 32;                                        // [blockDim]
   int* s_any = reinterpret_cast<int*>(s_incl + blockDim.x);
+  float* s_ps = reinterpret_cast<float*>(s_any + 4);               // [8][G] the slices' sums of each row
   int v0, v1;
   {
     v0 = (int)((long long)V * c / G);
@@ -2612,12 +2631,23 @@ __device__ __noinline__ bool head_select(const WindowBufs& W, const HeadArgs& H,
       float bv = -INFINITY;
       int bi = 0x7fffffff;
       bool fin = true;
-      for (int v = lo + lane; v < hi; v += 32) {
-        const float x = __ldcg(lg + v);
-        fin &= isfinite(x);
-        if (x > bv) {
-          bv = x;
-          bi = v;
+      for (int vb = lo; vb < hi; vb += 8 * 32) {  // eight loads in flight per lane
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int v = vb + u * 32 + lane;
+          x[u] = v < hi ? __ldcg(lg + v) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int v = vb + u * 32 + lane;
+          if (v < hi) {
+            fin &= isfinite(x[u]);
+            if (x[u] > bv) {
+              bv = x[u];
+              bi = v;
+            }
+          }
         }
       }
 #pragma unroll
@@ -2651,11 +2681,12 @@ __device__ __noinline__ bool head_select(const WindowBufs& W, const HeadArgs& H,
   if (!grid_barrier(W, s_ok)) return false;
   if (sampled) {
     // B: every CTA takes each row's maximum; this slice's sum of weights
-    if (tid < T) {
+    if (warp < T) {  // each row's maximum over the slices (warp t)
       float M = -INFINITY;
-#pragma unroll 8
-      for (int q = 0; q < G; ++q) M = fmaxf(M, __ldcg(H.part_max + q * kMaxRows + tid));
-      s_M[tid] = M;
+      for (int q = lane; q < G; q += 32) M = fmaxf(M, __ldcg(H.part_max + q * kMaxRows + warp));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      if (lane == 0) s_M[warp] = M;
     }
     __syncthreads();
     int a, b;
@@ -2669,26 +2700,30 @@ __device__ __noinline__ bool head_select(const WindowBufs& W, const HeadArgs& H,
     if (!grid_barrier(W, s_ok)) return false;
     // C: every CTA finds each sampled row's slice: the first whose running
     // total passes u x (the total); that CTA finds the token inside it
-    if (tid < T) {
+    if (warp < T) {  // row t = warp
       int cs = -1;
       float tl = 0.f;
-      if (H.temperature[tid] > 0.f) {
-        float Z = 0.f;
-        for (int q = 0; q < G; ++q) Z = __fadd_rn(Z, __ldcg(H.part_sum + q * kMaxRows + tid));
-        const float tgt = __fmul_rn(row_uniform((unsigned long long)(long long)H.position[tid], H.seed[tid]), Z);
-        float P = 0.f;
-        for (int q = 0; q < G; ++q) {
-          const float Pn = __fadd_rn(P, __ldcg(H.part_sum + q * kMaxRows + tid));
-          if (Pn > tgt) {
-            cs = q;
-            tl = __fsub_rn(tgt, P);
-            break;
+      if (H.temperature[warp] > 0.f) {
+        float* s_row = s_ps + warp * G;
+        const float Z = slice_total(H.part_sum, warp, G, s_row, lane);
+        if (lane == 0) {
+          const float tgt = __fmul_rn(row_uniform((unsigned long long)(long long)H.position[warp], H.seed[warp]), Z);
+          float P = 0.f;
+          for (int q = 0; q < G; ++q) {
+            const float Pn = __fadd_rn(P, s_row[q]);
+            if (Pn > tgt) {
+              cs = q;
+              tl = __fsub_rn(tgt, P);
+              break;
+            }
+            P = Pn;
           }
-          P = Pn;
         }
       }
-      s_cs[tid] = cs;
-      s_tgt[tid] = tl;
+      if (lane == 0) {
+        s_cs[warp] = cs;
+        s_tgt[warp] = tl;
+      }
     }
     __syncthreads();
     for (int t = 0; t < T; ++t) {
@@ -2721,27 +2756,35 @@ __device__ __noinline__ bool head_select(const WindowBufs& W, const HeadArgs& H,
   // final: CTA 0 writes the greedy tokens (and a sampled row's when no slice
   // passed its target), then each slot's emitted count
   if (c != 0) return true;
-  if (tid < T) {
-    const bool greedy = !(H.temperature[tid] > 0.f);
+  if (warp < T) {  // row t = warp
+    const bool greedy = !(H.temperature[warp] > 0.f);
     bool need = greedy;
     if (!greedy) {
-      float Z = 0.f;
-      for (int q = 0; q < G; ++q) Z = __fadd_rn(Z, __ldcg(H.part_sum + q * kMaxRows + tid));
-      const float tgt = __fmul_rn(row_uniform((unsigned long long)(long long)H.position[tid], H.seed[tid]), Z);
+      const float Z = slice_total(H.part_sum, warp, G, s_ps + warp * G, lane);
+      const float tgt = __fmul_rn(row_uniform((unsigned long long)(long long)H.position[warp], H.seed[warp]), Z);
       need = !(Z > tgt);
     }
-    if (need) {
+    if (need) {  // the argmax over the slices' maxima (ties to the lower token: any order gives the same)
       float bv = -INFINITY;
       int bi = 0x7fffffff;
-      for (int q = 0; q < G; ++q) {
-        const float v = __ldcg(H.part_max + q * kMaxRows + tid);
-        const int i = __ldcg(H.part_arg + q * kMaxRows + tid);
+      for (int q = lane; q < G; q += 32) {
+        const float v = __ldcg(H.part_max + q * kMaxRows + warp);
+        const int i = __ldcg(H.part_arg + q * kMaxRows + warp);
         if (better(v, i, bv, bi)) {
           bv = v;
           bi = i;
         }
       }
-      H.tokens[tid] = (bi >= 0 && bi < V) ? bi : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if (lane == 0) H.tokens[warp] = (bi >= 0 && bi < V) ? bi : 0;
     }
   }
   __syncthreads();
@@ -2784,14 +2827,20 @@ __global__ void __launch_bounds__(kExpertThreads, 1) head_kernel(LayerDev L, Win
     sW.rinv = s_rinv;
   }
   __syncthreads();
+  STAMP(0, 0);
   row_rinv(sW.x, sW.T, L.d, s_rinv);
   write_x_frags<BITS>(L, sW);
+  STAMP(0, 1);
   if (!grid_barrier(sW, &sp.ok)) return;
+  STAMP(0, 2);
   RingPos rp;
   int buf = 0;
   dense_phase<BITS, 2>(L, sW, C, sp, rg, m, rp, buf);
+  STAMP(0, 3);
   if (!grid_barrier(sW, &sp.ok) || s_abort) return;
+  STAMP(0, 4);
   head_select(sW, H, sW.q_out, &sp.ok, m.ring);
+  STAMP(0, 5);
 }
 
 // ---------------------------------------------------------------------------
