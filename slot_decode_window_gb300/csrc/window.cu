@@ -343,7 +343,19 @@ struct SPlan {
   int nfinish;
   int ok;                           // the grid barrier passed
   PhaseTasks pt[4];                 // gate/up, down, dense q/k/v, dense o
+  alignas(8) uint64_t img_bar;      // completion of a bulk copy of a B image into B
+  unsigned img_uses;                // copies completed so far (the wait's parity)
 };
+
+// The B-image copy barrier (thread 0, before the block barrier that follows
+// the kernel's set-up).
+__device__ __forceinline__ void init_img(SPlan& sp) {
+  if (threadIdx.x == 0) {
+    mbar_init(&sp.img_bar, 1);
+    sp.img_uses = 0;
+    fence_mbar_init();
+  }
+}
 
 __device__ __forceinline__ unsigned ord_f32(float f) {
   const unsigned u = __float_as_uint(f);
@@ -418,6 +430,7 @@ __device__ void write_x_frags(const LayerDev& L, const WindowBufs& W) {
       W.xfrag[ximg_sum(W.T, d, nmk, t, 1, off)] = lo;
     }
   }
+  asm volatile("fence.proxy.async.global;" ::: "memory");  // the image is read by bulk copies
 }
 
 // 1 / sqrt(mean(x_t^2) + 1e-6) of every row (warp t sums row t in a fixed
@@ -564,6 +577,7 @@ __device__ __noinline__ void router_stage(const LayerDev& L, const WindowBufs& W
       }
     }
   }
+  asm volatile("fence.proxy.async.global;" ::: "memory");  // the image is read by bulk copies
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < d / 16; i += blockDim.x) W.counters[i] = 0;
     for (int i = threadIdx.x; i <= E; i += blockDim.x) W.done_gu[i] = 0;
@@ -972,6 +986,40 @@ __device__ __forceinline__ void zero_padded_sums(__half* bs, const KernelCfg& C,
   }
 }
 
+// Copy a window's B image (global, set s of the main part at s * main_bytes,
+// of the sums at s * sum_bytes) into B (all consumer threads): thread 0 issues
+// one bulk copy per set and part, every thread waits (bounded) for them.  The
+// image was written by other CTAs' generic stores before a grid barrier, and B
+// last read by this CTA's generic loads before a consumer barrier: proxy
+// fences order both before the bulk copies.
+__device__ __forceinline__ void img_copy(SPlan& sp, __half* bm, __half* bs, int bmain_halves, int bsum_halves,
+                                         const __half* main_src, uint32_t main_bytes, const __half* sum_src,
+                                         uint32_t sum_bytes, int nsets, unsigned* err, long long wait_cycles, int ctid) {
+  const uint32_t parity = sp.img_uses & 1u;
+  if (ctid == 0) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(&sp.img_bar, (uint32_t)nsets * (main_bytes + sum_bytes));
+    for (int set = 0; set < nsets; ++set) {
+      bulk_g2s(bm + set * bmain_halves, main_src + (size_t)set * (main_bytes / 2), main_bytes, &sp.img_bar);
+      if (sum_bytes) bulk_g2s(bs + set * bsum_halves, sum_src + (size_t)set * (sum_bytes / 2), sum_bytes, &sp.img_bar);
+    }
+  }
+  // bounded by wait_cycles alone (the copies are in flight; an abort elsewhere
+  // does not stop them)
+  if (!mbar_try_wait(&sp.img_bar, parity)) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(&sp.img_bar, parity)) {
+      if (clock64() - t0 > wait_cycles) {
+        atomicOr(err, kErrTimeout);
+        break;
+      }
+    }
+  }
+  consumer_sync();  // every thread has seen this parity before the next copy flips it
+  if (ctid == 0) sp.img_uses += 1;
+}
+
 // Stage one group's activations into shared memory (all consumer threads).
 // Phases 0 and 2: copy x fragments (written by stage R or D0).  Phase 1: copy
 // h fragments (written by the gate/up epilogue) and form the block sums from
@@ -979,7 +1027,7 @@ __device__ __forceinline__ void zero_padded_sums(__half* bs, const KernelCfg& C,
 // pieces, all in flight before the one wait.  Phase 3 (the dense o
 // projection) forms v's fragments here, since v is short.
 template <int BITS, int PHASE>
-__device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan& sp, const KernelCfg& C, __half* bm,
+__device__ void load_group_B(const LayerDev& L, const WindowBufs& W, SPlan& sp, const KernelCfg& C, __half* bm,
                              __half* bs, bool is_shared, int R, int ent_off, int K, int ctid) {
   constexpr int S = Fmt<BITS>::kBHalves;
   constexpr int B = Fmt<BITS>::kBlock;
@@ -993,19 +1041,11 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
     TRACE(0, PHASE, 31, 0);
     const int T = W.T;
     if (PHASE == 2 || is_shared) {
-      // all T rows in order: the image is this group's B as it stands
-      const int per_set = 8 * K / 8;  // 16-byte pieces of one set's main part
-      for (int i = ctid; i < nsets * per_set; i += kConsumerThreads) {
-        const int set = i >= per_set ? 1 : 0, q = i - set * per_set;
-        cp_async16(bm + set * C.bmain_halves + q * 8, W.xfrag + (long long)set * 8 * K + q * 8);
-      }
+      // all T rows in order: the image is this group's B as it stands, one
+      // bulk copy per set of the main part and of the sums
+      img_copy(sp, bm, bs, C.bmain_halves, C.bsum_halves, W.xfrag, 16u * K, W.xfrag + 16LL * K, 256u * nmk, nsets,
+               W.err, W.wait_cycles, ctid);
       TRACE(0, PHASE, 31, 1);
-      const int sum_set = 32 * nmk;  // 8-byte pieces of one set's sums
-      for (int i = ctid; i < nsets * sum_set; i += kConsumerThreads) {
-        const int set = i >= sum_set ? 1 : 0, q = i - set * sum_set;
-        *reinterpret_cast<uint2*>(bs + set * C.bsum_halves + q * 4) =
-            __ldcg(reinterpret_cast<const uint2*>(W.xfrag + 16LL * K + (long long)set * 128 * nmk + q * 4));
-      }
     } else {
       // an expert's rows: each column's 16-byte pieces from its row's column
       // of the image
@@ -1111,10 +1151,7 @@ __device__ void load_group_B(const LayerDev& L, const WindowBufs& W, const SPlan
     // each written for every block of the broadcast input that repeats that v
     // block (the padded sum slots were cleared before the phase:
     // dense_o_prologue)
-    for (int i = ctid; i < nsets * K; i += kConsumerThreads) {  // K 16-byte pieces per set
-      const int set = i >= K ? 1 : 0, q = i - set * K;
-      cp_async16(bm + set * C.bmain_halves + q * 8, W.vimg + (long long)set * 8 * K + q * 8);
-    }
+    img_copy(sp, bm, nullptr, C.bmain_halves, 0, W.vimg, 16u * K, nullptr, 0u, nsets, W.err, W.wait_cycles, ctid);
     const int nbv = K / B;
     const int bph = (1 << L.kph_log2) * Fmt<BITS>::kBlocksPerKstep;
     const int ncopy = 1 << (L.kpg_log2 - L.kph_log2);
@@ -1472,6 +1509,7 @@ __device__ __forceinline__ void task_epilogue(const LayerDev& L, const WindowBuf
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) ps += __shfl_xor_sync(half_mask, ps, o);
             if (row == 0) atomicAdd(W.vsum + (long long)r * (L.dkv / B) + f / B, ps);
+            asm volatile("fence.proxy.async.global;" ::: "memory");  // the image is read by bulk copies
           }
         }
       } else if constexpr (PHASE == 3) {
@@ -2110,6 +2148,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) window_kernel(LayerDev L, W
   const Smem m = carve(smem, C);
   const Ring rg{m.ring, m.full, m.empty, &s_abort};
   init_cta(C, m, &s_abort);
+  init_img(sp);
   for (int i = threadIdx.x; i < 2 * kMaxExperts; i += blockDim.x) (&sp.wcnt[0][0])[i] = 0;
   STAMP(0, 0);
 
@@ -2145,6 +2184,7 @@ __global__ void __launch_bounds__(kConsumerThreads, 1) window_kernel_direct(Laye
   const Smem m = carve(smem, C);
   const Ring rg{m.ring, m.full, m.empty, &s_abort};
   init_cta(C, m, &s_abort);
+  init_img(sp);
   for (int i = threadIdx.x; i < 2 * kMaxExperts; i += blockDim.x) (&sp.wcnt[0][0])[i] = 0;
   router_stage<BITS>(L, W, reinterpret_cast<float*>(m.ring));
   if (!grid_barrier_split(W, &sp.ok, blockIdx.x == 0 && W.tier.counters != nullptr,
@@ -2408,6 +2448,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1)
   const Smem m = carve(smem, C);
   const Ring rg{m.ring, m.full, m.empty, &s_abort};
   init_cta(C, m, &s_abort);
+  init_img(sp);
   RingPos rp;
   int buf = 0;
   for (int l = 0; l < n_layers; ++l) {
@@ -2822,6 +2863,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) head_kernel(LayerDev L, Win
   const Smem m = carve(smem, C);
   const Ring rg{m.ring, m.full, m.empty, &s_abort};
   init_cta(C, m, &s_abort);
+  init_img(sp);
   if (threadIdx.x == 0) {
     sW = Wp;
     sW.rinv = s_rinv;
