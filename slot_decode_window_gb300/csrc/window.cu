@@ -1761,6 +1761,7 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
         enter_group<BITS, PHASE>(L, W, C, sp, tk, K, abort_flag, bm, bs, gs);
       }
       const ItemRange r = item_range<BITS, NS>(K, kg);
+      TRACE(0, PHASE, task - pt.t0, 0);
       float acc[4] = {0.f, 0.f, 0.f, 0.f}, accm[4] = {0.f, 0.f, 0.f, 0.f}, accm2[4] = {0.f, 0.f, 0.f, 0.f};
       const __half* bk = bm + r.k0 * 32 * S + gs.lane_b * 8;
       const __half* bsm = bs + r.m0 * 128 + gs.lane_b * 4;
@@ -1804,9 +1805,11 @@ __device__ void consume_direct(const LayerDev& L, const WindowBufs& W, const Ker
         bsm += 128;
         next_slot();
       }
+      TRACE(0, PHASE, task - pt.t0, 2);
       float4* rb = red + buf * (kConsumerWarps * 32);
       rb[warp * 32 + lane] = gs.paired ? partials<true>(acc, accm, accm2) : partials<false>(acc, accm, accm2);
       og.sync();
+      TRACE(0, PHASE, task - pt.t0, 3);
       {
         constexpr int kGT = OutGroup<PHASE, NS>::kThreads;
         const int i0 = og.id * 16 * gs.R;
@@ -2035,14 +2038,18 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
   if constexpr (DIRECT) {
     if (ns0 == 4) consume_direct<BITS, 0, 4>(L, W, C, sp, rg.abort_flag, m.bm, m.bs, m.red, m.ring, buf);
     else consume_direct<BITS, 0, 2>(L, W, C, sp, rg.abort_flag, m.bm, m.bs, m.red, m.ring, buf);
+    STAMP(0, 5);
     const bool slices = W.T < kGridCombineRows;  // else the caller combines after a grid barrier
     if (ns1 == 4) {
       consume_direct<BITS, 1, 4>(L, W, C, sp, rg.abort_flag, m.bm, m.bs, m.red, m.ring, buf);
+      STAMP(0, 8);
       if (slices) combine<4>(L, W, sp);
     } else {
       consume_direct<BITS, 1, 2>(L, W, C, sp, rg.abort_flag, m.bm, m.bs, m.red, m.ring, buf);
+      STAMP(0, 8);
       if (slices) combine<2>(L, W, sp);
     }
+    STAMP(0, 9);
     return true;
   }
   if (warp == kConsumerWarps) {
@@ -2186,16 +2193,21 @@ __global__ void __launch_bounds__(kConsumerThreads, 1) window_kernel_direct(Laye
   init_cta(C, m, &s_abort);
   init_img(sp);
   for (int i = threadIdx.x; i < 2 * kMaxExperts; i += blockDim.x) (&sp.wcnt[0][0])[i] = 0;
+  STAMP(0, 0);
   router_stage<BITS>(L, W, reinterpret_cast<float*>(m.ring));
+  STAMP(0, 1);
   if (!grid_barrier_split(W, &sp.ok, blockIdx.x == 0 && W.tier.counters != nullptr,
                           [&] { tier_round_due(W.tier, L.E, m.ring + kTierScratchOff); }))
     return;  // timed out: the error word says so
+  STAMP(0, 2);
   RingPos rp;
   int buf = 0;
   if (!moe_block<BITS, true>(L, W, C, sp, rg, m, rp, buf)) return;
   if (W.T >= kGridCombineRows) {
     if (!grid_barrier(W, &sp.ok) || s_abort) return;
+    STAMP(0, 10);
     combine_all(L, W);
+    STAMP(0, 16);
   }
 }
 
