@@ -582,6 +582,15 @@ def run_ours(args, rank, world, local_rank):
                                                 cpu_jobs if want_cpu else None)}
     stack = None if args.no_stack else measure_stack(args, dev, flush, stream, peak, cpu_jobs if want_cpu else None)
     clocks = sampler.stop()
+    # DRAM bytes per launch from the committed ncu summaries (null when the
+    # kernel source changed since they were taken)
+    if workloads:
+        for wl_name, entry in workloads.items():
+            if "8" in entry:
+                entry["8"]["traffic"] = profiled_traffic("window_kernel_direct", wl_name)
+    if stack:
+        t2 = profiled_traffic("stack_kernel", "stack48_2layers")
+        stack["traffic_per_layer"] = t2 / 2 if t2 is not None else None
 
     cpu = cpu_all = None
     if want_cpu:
@@ -656,7 +665,8 @@ def measure_head(dev, flush, peak, steps=200):
             "kernel": "head_kernel<4> (RMSNorm, head GEMV, draw, proposal check; one cooperative launch)",
             "us_per_window_mean": 1e6 * mean_s, "us_per_window_p10": 1e3 * q10, "us_per_window_median": 1e3 * q50,
             "us_per_window_p90": 1e3 * q90, "algorithmic_bytes": nbytes, "achieved_GBps": nbytes / mean_s / 1e9,
-            "frac_of_measured_hbm": nbytes / mean_s / 1e9 / peak, "rows_per_s": T / mean_s}
+            "frac_of_measured_hbm": nbytes / mean_s / 1e9 / peak, "rows_per_s": T / mean_s,
+            "traffic": profiled_traffic("head_kernel", "d2048_v151936")}
 
 
 def measure_tier(win, X, Y, T, flush, steps):
