@@ -157,3 +157,36 @@ def test_stack48_full_depth_rows_and_determinism():
                 break
     assert checked >= 3, f"only {checked} rows kept a 1e-3 margin at every layer"
     stk.close()
+
+
+def test_windows_of_other_sizes_leave_no_trace():
+    """The x and v B images keep each window's rows in the layout of its own
+    size (paired columns up to 4 rows, two sets above), so a window that
+    follows windows of other sizes on the same handle must give the same bits
+    as on a fresh handle: an 8-row window, then 3- and 1-row windows, then the
+    8-row window again, and the 3-row window against a fresh handle."""
+    from slot_decode_window_gb300 import binding
+    wl = wlm.Workload("stack_small", 93, wlm.MoESpec(256, 8, 2, 128, 128, 4, 32), (1,), n_layers=2,
+                      heads=4, kv_heads=2, head_dim=64)
+    moe, dense = _layers(wl, 2)
+    x8 = torch.from_numpy(wlm.make_window(wl, 8, seed=0, window=11)).cuda()
+    x3 = torch.from_numpy(wlm.make_window(wl, 3, seed=0, window=12)).cuda()
+    x1 = torch.from_numpy(wlm.make_window(wl, 1, seed=0, window=13)).cuda()
+    stk = binding.Stack(wl, moe, dense, max_rows=8)
+    try:
+        a = stk.forward(x8).clone()
+        b = stk.forward(x3).clone()
+        stk.forward(x1)
+        a2 = stk.forward(x8).clone()
+        stk.sync()
+    finally:
+        stk.close()
+    fresh = binding.Stack(wl, moe, dense, max_rows=8)
+    try:
+        b2 = fresh.forward(x3).clone()
+        fresh.sync()
+    finally:
+        fresh.close()
+    assert torch.isfinite(a).all() and torch.isfinite(b).all()
+    assert torch.equal(a, a2)
+    assert torch.equal(b, b2)
