@@ -911,7 +911,11 @@ __device__ __forceinline__ int task_cost(int R) { return R <= 4 ? 2 : 3; }
 // Contiguous task ranges of equal estimated cost (one warp): each lane takes a
 // run of consecutive groups, a warp scan gives every group its starting cost
 // position, and the lane whose groups hold a range boundary reports the task.
-__device__ __forceinline__ void split_tasks(const WindowBufs& W, SPlan& sp, bool has_shared, PhaseTasks& pt, int lane) {
+// group_cost: the estimated cost of staging a group's activations, in the
+// same units, charged to the group's first task (measured per CTA on GB300:
+// ~0.45 of a paired 4-bit task in both phases; small beside a 2-bit task).
+__device__ __forceinline__ void split_tasks(const WindowBufs& W, SPlan& sp, bool has_shared, PhaseTasks& pt, int lane,
+                                            int group_cost) {
   const int hs = has_shared ? 1 : 0;
   const int ng = hs + sp.nd;
   const int ntotal = hs * pt.ntask_s + sp.nd * pt.ntask_e;
@@ -928,7 +932,7 @@ __device__ __forceinline__ void split_tasks(const WindowBufs& W, SPlan& sp, bool
     if (g < ng) {
       int nt, cst;
       cost_of(g, nt, cst);
-      run += nt * cst;
+      run += nt * cst + group_cost;
     }
   }
   int incl = run;
@@ -948,10 +952,11 @@ __device__ __forceinline__ void split_tasks(const WindowBufs& W, SPlan& sp, bool
       if (g < ng) {
         int nt, cst;
         cost_of(g, nt, cst);
-        const int len = nt * cst;
+        const int len = nt * cst + group_cost;
         if (P >= pos && P < pos + len) {
           const int first = (g < hs) ? 0 : hs * pt.ntask_s + (g - hs) * pt.ntask_e;
-          const int j = (P - pos + cst - 1) / cst;
+          const int into = P - pos - group_cost;
+          const int j = into <= 0 ? 0 : (into + cst - 1) / cst;
           found = first + (j < nt ? j : nt);
         }
         pos += len;
@@ -2009,7 +2014,7 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
     p0.mt = (C.ph[0].max_sub >= 4 && tiles_e % 2 == 0 && tiles_s % 2 == 0) ? 2 : 1;
     p0.ntask_s = tiles_s / p0.mt;
     p0.ntask_e = tiles_e / p0.mt;
-    split_tasks(W, sp, has_shared, p0, lane);
+    split_tasks(W, sp, has_shared, p0, lane, BITS == 4 ? 2 : 0);
   } else if (warp == 1) {
     // down: as many row tiles per task (up to 4) as the stage plan allows and
     // the d / 16 row tiles divide into (a down task is short, and its fixed
@@ -2022,7 +2027,7 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
     p1.mt = mt;
     p1.ntask_s = has_shared ? tiles_g / mt : 0;
     p1.ntask_e = tiles_g / mt;
-    split_tasks(W, sp, has_shared, p1, lane);
+    split_tasks(W, sp, has_shared, p1, lane, BITS == 4 ? 2 : 0);
   }
   __syncthreads();
 #ifdef STRATA_STAMPS
