@@ -905,8 +905,9 @@ __device__ __forceinline__ Task decode_task(int task, const PhaseTasks& pt, bool
 }
 
 // Estimated cost of one task of a group of R rows (groups of more than 4 rows
-// take the two-set path: twice the MMAs and activation loads).
-__device__ __forceinline__ int task_cost(int R) { return R <= 4 ? 2 : 3; }
+// take the two-set path: twice the MMAs and activation loads); a paired task
+// costs 2, a two-set one two_set.
+__device__ __forceinline__ int task_cost(int R, int two_set) { return R <= 4 ? 2 : two_set; }
 
 // Contiguous task ranges of equal estimated cost (one warp): each lane takes a
 // run of consecutive groups, a warp scan gives every group its starting cost
@@ -915,7 +916,7 @@ __device__ __forceinline__ int task_cost(int R) { return R <= 4 ? 2 : 3; }
 // same units, charged to the group's first task (measured per CTA on GB300:
 // ~0.45 of a paired 4-bit task in both phases; small beside a 2-bit task).
 __device__ __forceinline__ void split_tasks(const WindowBufs& W, SPlan& sp, bool has_shared, PhaseTasks& pt, int lane,
-                                            int group_cost) {
+                                            int group_cost, int two_set) {
   const int hs = has_shared ? 1 : 0;
   const int ng = hs + sp.nd;
   const int ntotal = hs * pt.ntask_s + sp.nd * pt.ntask_e;
@@ -924,7 +925,7 @@ __device__ __forceinline__ void split_tasks(const WindowBufs& W, SPlan& sp, bool
   auto cost_of = [&](int g, int& nt, int& cst) {
     const bool sh = has_shared && g == 0;
     nt = sh ? pt.ntask_s : pt.ntask_e;
-    cst = task_cost(sh ? W.T : sp.counts[sp.distinct[g - hs]]);
+    cst = task_cost(sh ? W.T : sp.counts[sp.distinct[g - hs]], two_set);
   };
   int run = 0;
   for (int i = 0; i < per; ++i) {
@@ -2014,7 +2015,7 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
     p0.mt = (C.ph[0].max_sub >= 4 && tiles_e % 2 == 0 && tiles_s % 2 == 0) ? 2 : 1;
     p0.ntask_s = tiles_s / p0.mt;
     p0.ntask_e = tiles_e / p0.mt;
-    split_tasks(W, sp, has_shared, p0, lane, BITS == 4 ? 2 : 0);
+    split_tasks(W, sp, has_shared, p0, lane, BITS == 4 ? 2 : 0, 3);
   } else if (warp == 1) {
     // down: as many row tiles per task (up to 4) as the stage plan allows and
     // the d / 16 row tiles divide into (a down task is short, and its fixed
@@ -2027,7 +2028,9 @@ __device__ __forceinline__ bool moe_block(const LayerDev& L, const WindowBufs& W
     p1.mt = mt;
     p1.ntask_s = has_shared ? tiles_g / mt : 0;
     p1.ntask_e = tiles_g / mt;
-    split_tasks(W, sp, has_shared, p1, lane, BITS == 4 ? 2 : 0);
+    // (a two-set down task costs ~1.9 paired ones on the ring path, ~1.5 on
+    // the warp-streamed one: measured per CTA)
+    split_tasks(W, sp, has_shared, p1, lane, BITS == 4 ? 2 : 0, DIRECT ? 3 : 4);
   }
   __syncthreads();
 #ifdef STRATA_STAMPS
