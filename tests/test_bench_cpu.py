@@ -82,3 +82,29 @@ def test_reference_arm_under_two_ranks_prints_once():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
+def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    """A committed ncu summary's DRAM bytes are reported only while its
+    source_sha1 matches the kernel source; every kernel summary carries both
+    lines and the command that made it."""
+    import bench
+    prof = os.path.join(bench.ROOT, "profiles")
+    names = [f for f in os.listdir(prof) if f.endswith(".md") and not f.startswith("launches")]
+    assert names
+    for f in names:
+        text = open(os.path.join(prof, f)).read()
+        assert "ncu --set full --clock-control none" in text, f
+        assert any(l.startswith("traffic_bytes_per_launch:") for l in text.splitlines()), f
+        assert any(l.startswith("source_sha1:") for l in text.splitlines()), f
+    # a summary whose hash matches is read; one whose hash does not is ignored
+    sha = bench.kernel_source_hash()
+    fake = tmp_path / "profiles"
+    fake.mkdir()
+    (fake / "k_w.md").write_text(f"x\ntraffic_bytes_per_launch: 1234\nsource_sha1: {sha}\n")
+    (fake / "k_old.md").write_text("x\ntraffic_bytes_per_launch: 99\nsource_sha1: 000000000000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: sha)
+    assert bench.profiled_traffic("k", "w") == 1234.0
+    assert bench.profiled_traffic("k", "old") is None
+    assert bench.profiled_traffic("k", "missing") is None
